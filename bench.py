@@ -1,0 +1,351 @@
+"""Benchmark of the PolyKV hot path: encode the shared pool, then run
+multi-agent decode attention over it, on synthetic inputs of the
+Llama-3-8B shape (32 layers, 8 kv heads, 32 q heads, head_dim 128, bf16,
+4096-token shared context, 15 agents).
+
+A step = one encode of the whole context (keys -> q8_0, values -> FWHT +
+3-bit codes) + one decode attention of every agent's query over the pool.
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "pool decode-attention HBM GB/s (% of peak) & encode tokens/s, Llama-3-8B shape"
+DEFAULT_WORKLOAD = "llama3_8b_4096_a15"
+
+
+def algorithmic_bytes(w: synth.Workload, n_ctx: int, n_agents: int):
+    """(encode bytes, attend bytes) per call, from the pool format."""
+    L, H, Hq, d = w.n_layers, w.n_kv_heads, w.n_q_heads, w.head_dim
+    per_tok_pool = d + 2 * (d // 32) + 3 * d // 8 + 2
+    pool = L * H * n_ctx * per_tok_pool
+    enc = L * H * n_ctx * d * 2 * 2 + pool          # read K, V (16-bit), write the pool
+    att = pool + L * n_agents * Hq * d * 2 + L * n_agents * Hq * d * 4   # pool + q + fp32 out
+    return enc, att
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "serving_q8_encode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str, workload: str, src_hash: str):
+    """Per-launch DRAM bytes recorded from an ncu capture, if the kernel's source
+    has not changed since (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    e = j.get(kernel, {}).get(workload)
+    if not e or e.get("src_hash") != src_hash:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, w: synth.Workload):
+    """The CPU oracle, timed as it stands, on a bounded sample per step."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    c32, b32 = oracle.codebook.codebook_f32()
+    sample_layers = 1
+    kb, vb = synth.gen_kv(sample_layers, w.n_kv_heads, w.n_ctx, w.head_dim, w.dtype, 0)
+    qb = synth.gen_q(sample_layers, w.n_agents, w.n_q_heads, w.head_dim, w.dtype, 0)
+    enc_b, att_b = algorithmic_bytes(w, w.n_ctx, w.n_agents)
+    frac = sample_layers / w.n_layers
+    sample_bytes = (enc_b + att_b) * frac
+
+    def step():
+        pool = oracle.attention.encode_pool(kb, vb, w.dtype, b32)
+        oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sample_bytes / dt / 1e9
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(w.describe(), sample=f"{sample_layers} of {w.n_layers} layers per step"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"encode + attend of {sample_layers} layer(s) x {w.n_kv_heads} kv heads x "
+                                   f"{w.n_ctx} tokens x {w.n_agents} agents per step; numpy (BLAS may thread)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(w: synth.Workload):
+    """Oracle timed on a bounded sample (1 layer) of the workload, scaled to GB/s."""
+    import oracle
+    c32, b32 = oracle.codebook.codebook_f32()
+    kb, vb = synth.gen_kv(1, w.n_kv_heads, w.n_ctx, w.head_dim, w.dtype, 0)
+    qb = synth.gen_q(1, w.n_agents, w.n_q_heads, w.head_dim, w.dtype, 0)
+    enc_b, att_b = algorithmic_bytes(w, w.n_ctx, w.n_agents)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        pool = oracle.attention.encode_pool(kb, vb, w.dtype, b32)
+        oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 20:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": (enc_b + att_b) / w.n_layers / dt / 1e9, "unit": "GB/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{reps} x (encode + attend of 1 of {w.n_layers} layers, all heads/agents); numpy, "
+                      f"BLAS threads up to the core count"}
+
+
+# ----------------------------------------------------------------------------- polykv arm
+def run_polykv(args, w: synth.Workload):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import serving_q8_encode_gb300 as pk
+
+    L, H, Hq, d, T, A = w.n_layers, w.n_kv_heads, w.n_q_heads, w.head_dim, w.n_ctx, w.n_agents
+    kb, vb = synth.gen_kv(L, H, T, d, w.dtype, seed=rank)
+    qb = synth.gen_q(L, A, Hq, d, w.dtype, seed=rank)
+    k = torch.from_numpy(kb.view(np.int16)).to(dev)
+    v = torch.from_numpy(vb.view(np.int16)).to(dev)
+    q = torch.from_numpy(qb.view(np.int16)).to(dev)
+    pool = pk.Pool(L, H, d, T, w.dtype, device=dev)
+    out = torch.empty((L, A, Hq, d), dtype=torch.float32, device=dev)
+    pool.encode(k, v)  # so the prefix is valid for the workspace query
+    ws = torch.empty(max(16, pool.workspace_size(A, Hq, T)), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pool.encode(k, v, stream=stream)
+        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(float(i))  # L2 flush between steps (outside the events)
+        ev[i][0].record(stream)
+        pool.encode(k, v, stream=stream)
+        ev[i][1].record(stream)
+        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    enc_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    att_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = float(np.mean([a + b for a, b in zip(enc_ms, att_ms)]))
+    enc_ms_m, att_ms_m = float(np.mean(enc_ms)), float(np.mean(att_ms))
+
+    # attention alone, L2 flushed before each launch (the pool is read from HBM)
+    att_alone = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        att_alone.append(e0.elapsed_time(e1))
+    att_alone_ms = float(np.mean(att_alone))
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    hk = torch.from_numpy(kb.view(np.int16)).pin_memory()
+    hv = torch.from_numpy(vb.view(np.int16)).pin_memory()
+    hq = torch.from_numpy(qb.view(np.int16)).pin_memory()
+    hout = torch.empty((L, A, Hq, d), dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(max(2, args.steps // 2) + 1):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        q.copy_(hq, non_blocking=True)
+        pool.encode(k, v, stream=stream)
+        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        if i > 0:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_ms_m = float(np.mean(e2e_ms))
+
+    def allmax(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    step_ms = allmax(step_ms)
+    enc_ms_m = allmax(enc_ms_m)
+    att_ms_m = allmax(att_ms_m)
+    att_alone_ms = allmax(att_alone_ms)
+    e2e_ms_m = allmax(e2e_ms_m)
+
+    enc_b, att_b = algorithmic_bytes(w, T, A)
+    peak, peak_src = measured_peaks()
+    value = world * (enc_b + att_b) / (step_ms * 1e-3) / 1e9
+    att_gbs = att_b / (att_alone_ms * 1e-3) / 1e9
+    enc_gbs = enc_b / (enc_ms_m * 1e-3) / 1e9
+    enc_tok_s = world * T / (enc_ms_m * 1e-3)
+    dominant = "encode" if enc_ms_m >= att_ms_m else "attend"
+    if dominant == "encode":
+        kname, kbytes, kms, files = "encode_kernel", enc_b, enc_ms_m, ["encode.cu"]
+    else:
+        kname, kbytes, kms, files = "attend", att_b, att_ms_m, ["attend_simt.cu"]
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    traffic = traffic_from_profiles(kname, w.name, kernel_source_hash(files))
+    att_traffic = traffic_from_profiles("attend", w.name, kernel_source_hash(["attend_simt.cu"]))
+    h2d = kb.nbytes + vb.nbytes + qb.nbytes
+    d2h = L * A * Hq * d * 4
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16->u8/i8 codes, f32 accumulate", "data": "synthetic",
+        "config": dict(w.describe(), l2="flushed between steps (2x L2 write)",
+                       step="encode whole context + attend all agents", parallelism=f"replicas x{world}"),
+        "attend": {"gbs": att_gbs, "frac_of_peak": att_gbs / peak, "us": att_alone_ms * 1e3,
+                   "us_in_step": att_ms_m * 1e3, "bytes": att_b, "traffic": att_traffic},
+        "encode": {"tokens_per_s": enc_tok_s, "gbs": enc_gbs, "frac_of_peak": enc_gbs / peak,
+                   "us": enc_ms_m * 1e3, "bytes": enc_b},
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs"},
+        "e2e": {"value": world * (enc_b + att_b) / (e2e_ms_m * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_m},
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="polykv", choices=["polykv", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_polykv(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

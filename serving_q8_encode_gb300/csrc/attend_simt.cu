@@ -1,0 +1,400 @@
+// Multi-agent decode attention over the shared pool on CUDA cores (any number
+// of query rows; the general path and the one used when few rows share a kv
+// head).
+//
+// PolyKV abstract ("PolyKV: A Shared Asymmetrically-Compressed KV Cache Pool
+// for Multi-Agent LLM Inference"): N agents read one compressed pool. Each
+// CTA owns one (layer, kv head, token split) and ALL query rows that read
+// that kv head (agents x GQA group), so every pool byte is fetched once per
+// split for all agents. Keys are dequantized in registers (int8 code times
+// the block's fp16 scale, applied to the 32-wide partial dot product); the
+// online softmax runs in base 2; values are accumulated in the ROTATED basis
+// as p * ||v|| * centroid[code]. Because the inverse transform is linear, the
+// merge kernel applies one inverse FWHT per output row instead of one per
+// value vector:  o = (1/d) H (sum_t p_t n_t C[code_t]) / sum_t p_t.
+#include <algorithm>
+#include <cmath>
+
+#include "polykv_internal.cuh"
+
+namespace polykv {
+namespace {
+
+constexpr int kTT = 64;        // tokens per tile
+constexpr int kThreads = 128;
+constexpr int kMaxRowsPerCta = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float centroid_signed(uint32_t code) {
+    const uint32_t idx = code >= 4 ? code - 4 : 3 - code;
+    const float m = idx == 0 ? kC4 : (idx == 1 ? kC5 : (idx == 2 ? kC6 : kC7));
+    return code >= 4 ? m : -m;
+}
+
+__device__ __forceinline__ float q_to_float(uint16_t bits, bool bf16) {
+    return bf16 ? __uint_as_float((uint32_t)bits << 16) : __half2float(__ushort_as_half(bits));
+}
+
+template <int D, int RMAX>
+struct SimtSmem {
+    static constexpr int kQs = D * RMAX;            // [D][RMAX]
+    static constexpr int kSc = RMAX * (kTT + 1);    // [RMAX][kTT+1]
+    static constexpr int kVh = kTT * (D + 4);       // [kTT][D+4]
+    static constexpr int kFloats = kQs + kSc + kVh + 3 * RMAX;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+// grid: (split, unit = layer*H + kv_head, row chunk); block: 128 threads.
+template <int D, int RMAX, bool BF16>
+__global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, const uint16_t* __restrict__ q, int A,
+                                                                int Hq, int R, int64_t n_ctx, int64_t split_len,
+                                                                int n_splits, float scale_log2, float* __restrict__ ws_acc,
+                                                                float* __restrict__ ws_ml) {
+    using S = SimtSmem<D, RMAX>;
+    extern __shared__ float4 smem4[];
+    float* smem = reinterpret_cast<float*>(smem4);
+    float* qs = smem;                 // [D][RMAX]
+    float* sc = qs + S::kQs;          // [RMAX][kTT+1]
+    float* vh = sc + S::kSc;          // [kTT][D+4]
+    float* m_s = vh + S::kVh;
+    float* l_s = m_s + RMAX;
+    float* al_s = l_s + RMAX;
+
+    const int tid = threadIdx.x;
+    const int split = blockIdx.x;
+    const int unit = blockIdx.y;
+    const int row0 = blockIdx.z * RMAX;
+    const int nrows = min(RMAX, R - row0);
+    const int layer = unit / p.H, kvh = unit % p.H;
+    const int G = Hq / p.H;
+
+    // ---- query rows of this kv head, transposed to [j][r], fp32
+    for (int i = tid; i < D * RMAX; i += kThreads) {
+        const int r = i / D, j = i % D;
+        float val = 0.0f;
+        if (r < nrows) {
+            const int gr = row0 + r;
+            const int a = gr / G, g = gr % G;
+            val = q_to_float(q[(((int64_t)layer * A + a) * Hq + kvh * G + g) * D + j], BF16);
+        }
+        qs[j * RMAX + r] = val;
+    }
+    if (tid < RMAX) {
+        m_s[tid] = -INFINITY;
+        l_s[tid] = 0.0f;
+    }
+
+    const int64_t t_begin = (int64_t)split * split_len;
+    const int64_t t_end = (t_begin + split_len < n_ctx) ? t_begin + split_len : n_ctx;
+    const int64_t ubase = (int64_t)unit * p.cap;
+
+    // PV mapping: column quad cq, row group rg
+    constexpr int NCQ = D / 4;
+    constexpr int NRG = kThreads / NCQ;
+    constexpr int ROWS = (RMAX + NRG - 1) / NRG;
+    const int cq = tid % NCQ, rg = tid / NCQ;
+    float acc[ROWS][4];
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[i][c] = 0.0f;
+
+    __syncthreads();
+
+    for (int64_t tile = t_begin; tile < t_end; tile += kTT) {
+        // ---- A: scores, thread = (token, row half)
+        {
+            constexpr int RH = RMAX / 2;
+            const int t = tid % kTT, rh = tid / kTT;
+            const int64_t tok = tile + t;
+            const bool valid = tok < t_end;
+            float score[RH];
+#pragma unroll
+            for (int i = 0; i < RH; ++i) score[i] = 0.0f;
+            if (valid) {
+                const uint4* krow = reinterpret_cast<const uint4*>(p.kq + (ubase + tok) * D);
+                const __half* srow = p.ks + (ubase + tok) * (D / kQ8Block);
+#pragma unroll
+                for (int b = 0; b < D / kQ8Block; ++b) {
+                    float part[RH];
+#pragma unroll
+                    for (int i = 0; i < RH; ++i) part[i] = 0.0f;
+#pragma unroll
+                    for (int w16 = 0; w16 < 2; ++w16) {
+                        const uint4 kr = krow[b * 2 + w16];
+                        const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float kf = (float)(int8_t)((kw[e >> 2] >> (8 * (e & 3))) & 0xFF);
+                            const int j = b * 32 + w16 * 16 + e;
+                            const float* qj = qs + j * RMAX + rh * RH;
+#pragma unroll
+                            for (int i = 0; i < RH; i += 4) {
+                                const float4 q4 = *reinterpret_cast<const float4*>(qj + i);
+                                part[i] = fmaf(q4.x, kf, part[i]);
+                                part[i + 1] = fmaf(q4.y, kf, part[i + 1]);
+                                part[i + 2] = fmaf(q4.z, kf, part[i + 2]);
+                                part[i + 3] = fmaf(q4.w, kf, part[i + 3]);
+                            }
+                        }
+                    }
+                    const float sb = __half2float(srow[b]);
+#pragma unroll
+                    for (int i = 0; i < RH; ++i) score[i] = fmaf(sb, part[i], score[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RH; ++i) {
+                const int r = rh * RH + i;
+                if (r < nrows) sc[r * (kTT + 1) + t] = valid ? score[i] * scale_log2 : -INFINITY;
+            }
+        }
+        // ---- C: dequantize the value tile to n * centroid[code] (rotated basis)
+        {
+            const int t = tid / 2, half = tid % 2;
+            const int64_t tok = tile + t;
+            const bool valid = tok < t_end;
+            float* dst = vh + t * (D + 4) + half * (D / 2);
+            if (valid) {
+                const float nv = __half2float(p.vn[ubase + tok]);
+                const uint32_t* cw =
+                    reinterpret_cast<const uint32_t*>(p.vc + (ubase + tok) * (3 * D / 8) + half * (3 * D / 16));
+                constexpr int NW = 3 * D / 64;   // 32-bit words per half row
+                uint32_t w[NW];
+#pragma unroll
+                for (int i = 0; i < NW; ++i) w[i] = cw[i];
+#pragma unroll
+                for (int g8 = 0; g8 < D / 16; ++g8) {  // 8-code groups in this half
+                    // bytes 3*g8 .. 3*g8+2 of the half row
+                    uint32_t w24 = 0;
+#pragma unroll
+                    for (int bb = 0; bb < 3; ++bb) {
+                        const int byte = 3 * g8 + bb;
+                        w24 |= ((w[byte >> 2] >> (8 * (byte & 3))) & 0xFF) << (8 * bb);
+                    }
+                    float4 lo, hi;
+                    lo.x = nv * centroid_signed((w24 >> 0) & 7);
+                    lo.y = nv * centroid_signed((w24 >> 3) & 7);
+                    lo.z = nv * centroid_signed((w24 >> 6) & 7);
+                    lo.w = nv * centroid_signed((w24 >> 9) & 7);
+                    hi.x = nv * centroid_signed((w24 >> 12) & 7);
+                    hi.y = nv * centroid_signed((w24 >> 15) & 7);
+                    hi.z = nv * centroid_signed((w24 >> 18) & 7);
+                    hi.w = nv * centroid_signed((w24 >> 21) & 7);
+                    reinterpret_cast<float4*>(dst)[2 * g8] = lo;
+                    reinterpret_cast<float4*>(dst)[2 * g8 + 1] = hi;
+                }
+            } else {
+                for (int i = 0; i < D / 8; ++i) reinterpret_cast<float4*>(dst)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        __syncthreads();
+        // ---- B: online softmax per row (base 2), warp per row
+        {
+            const int warp = tid / 32, lane = tid % 32;
+            for (int r = warp; r < nrows; r += kThreads / 32) {
+                float* row = sc + r * (kTT + 1);
+                const float x0 = row[lane], x1 = row[lane + 32];
+                float mt = fmaxf(x0, x1);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                const float m_old = m_s[r];
+                const float m_new = fmaxf(m_old, mt);
+                float p0 = 0.f, p1 = 0.f, alpha = 1.f;
+                if (m_new != -INFINITY) {
+                    p0 = exp2f(x0 - m_new);
+                    p1 = exp2f(x1 - m_new);
+                    alpha = exp2f(m_old - m_new);
+                }
+                float sum = p0 + p1;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                row[lane] = p0;
+                row[lane + 32] = p1;
+                if (lane == 0) {
+                    l_s[r] = l_s[r] * alpha + sum;
+                    m_s[r] = m_new;
+                    al_s[r] = alpha;
+                }
+            }
+        }
+        __syncthreads();
+        // ---- D: acc[r][:] = acc * alpha + sum_t p[r][t] * vh[t][:]
+        {
+#pragma unroll
+            for (int i = 0; i < ROWS; ++i) {
+                const int r = rg * ROWS + i;
+                if (r < nrows) {
+                    const float a = al_s[r];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[i][c] *= a;
+                }
+            }
+            const int tmax = (t_end - tile < kTT) ? (int)(t_end - tile) : kTT;
+            for (int t = 0; t < tmax; ++t) {
+                const float4 vv = reinterpret_cast<const float4*>(vh + t * (D + 4))[cq];
+#pragma unroll
+                for (int i = 0; i < ROWS; ++i) {
+                    const int r = rg * ROWS + i;
+                    if (r < nrows) {
+                        const float pr = sc[r * (kTT + 1) + t];
+                        acc[i][0] = fmaf(pr, vv.x, acc[i][0]);
+                        acc[i][1] = fmaf(pr, vv.y, acc[i][1]);
+                        acc[i][2] = fmaf(pr, vv.z, acc[i][2]);
+                        acc[i][3] = fmaf(pr, vv.w, acc[i][3]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- partials: acc [U][S][R][D], (m, l) [U][S][R][2]
+    const int64_t pbase = ((int64_t)unit * n_splits + split) * R;
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+        const int r = rg * ROWS + i;
+        if (r < nrows)
+            reinterpret_cast<float4*>(ws_acc + (pbase + row0 + r) * D)[cq] =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+    if (tid < nrows) {
+        ws_ml[(pbase + row0 + tid) * 2] = m_s[tid];
+        ws_ml[(pbase + row0 + tid) * 2 + 1] = l_s[tid];
+    }
+}
+
+// One warp per (unit, row): log-sum-exp merge of the splits, normalisation,
+// one inverse FWHT of the row (o = (1/d) H acc / l), fp32 output.
+template <int D>
+__global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
+                                                    float* __restrict__ out, int U, int H, int A, int Hq, int R,
+                                                    int n_splits) {
+    constexpr int EPL = D / 32;  // elements per lane
+    const int wid = blockIdx.x * 4 + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (wid >= U * R) return;
+    const int unit = wid / R, r = wid % R;
+    const int G = Hq / H;
+    const int layer = unit / H, kvh = unit % H;
+    const int a = r / G, g = r % G;
+
+    float M = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[(((int64_t)unit * n_splits + s) * R + r) * 2]);
+    float L = 0.0f;
+    float o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
+    for (int s = 0; s < n_splits; ++s) {
+        const int64_t pr = ((int64_t)unit * n_splits + s) * R + r;
+        const float ms = ws_ml[pr * 2];
+        if (ms == -INFINITY) continue;
+        const float w = exp2f(ms - M);
+        L = fmaf(w, ws_ml[pr * 2 + 1], L);
+        const float* src = ws_acc + pr * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, src[e], o[e]);
+    }
+    const float inv = 1.0f / L;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] *= inv;
+    // in-lane butterflies (strides < EPL), then across lanes
+#pragma unroll
+    for (int h = 1; h < EPL; h <<= 1)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+            if ((e & h) == 0) {
+                const float x = o[e], y = o[e + h];
+                o[e] = x + y;
+                o[e + h] = x - y;
+            }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const float other = __shfl_xor_sync(0xffffffffu, o[e], m);
+            o[e] = upper ? other - o[e] : o[e] + other;
+        }
+    }
+    float* dst = out + (((int64_t)layer * A + a) * Hq + kvh * G + g) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dst[e] = o[e] * (1.0f / D);
+}
+
+template <int D, int RMAX, bool BF16>
+polykv_status run_simt(const PoolView& p, const void* q, float* out, int A, int Hq, int R, int64_t n_ctx,
+                       float scale, float* ws, int n_splits, int64_t split_len, cudaStream_t st) {
+    using S = SimtSmem<D, RMAX>;
+    auto kern = attend_partial_simt<D, RMAX, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend: smem attribute: %s", cudaGetErrorString(e));
+    const int U = p.L * p.H;
+    float* ws_acc = ws;
+    float* ws_ml = ws + (size_t)U * n_splits * R * D;
+    dim3 grid(n_splits, U, (R + RMAX - 1) / RMAX);
+    kern<<<grid, kThreads, S::kBytes, st>>>(p, static_cast<const uint16_t*>(q), A, Hq, R, n_ctx, split_len, n_splits,
+                                            scale * kLog2e, ws_acc, ws_ml);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend partial launch: %s", cudaGetErrorString(e));
+    const int warps = U * R;
+    attend_merge<D><<<(warps + 3) / 4, 128, 0, st>>>(ws_acc, ws_ml, out, U, p.H, A, Hq, R, n_splits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend merge launch: %s", cudaGetErrorString(e));
+    return POLYKV_OK;
+}
+
+template <int D, bool BF16>
+polykv_status dispatch_rows(const PoolView& p, const void* q, float* out, int A, int Hq, int R, int64_t n_ctx,
+                            float scale, float* ws, int n_splits, int64_t split_len, cudaStream_t st) {
+    if (R <= 8) return run_simt<D, 8, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
+    if (R <= 16) return run_simt<D, 16, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
+    if (R <= 32) return run_simt<D, 32, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
+    return run_simt<D, kMaxRowsPerCta, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
+}
+
+int64_t split_length(const PoolView& p, int rows, int64_t n_ctx) {
+    const int U = p.L * p.H;
+    const int chunks = (rows + kMaxRowsPerCta - 1) / kMaxRowsPerCta;
+    const int64_t want_ctas = 4 * 152;
+    int64_t s = (want_ctas + (int64_t)U * chunks - 1) / ((int64_t)U * chunks);
+    const int64_t tiles = (n_ctx + kTT - 1) / kTT;
+    s = std::max<int64_t>(1, std::min<int64_t>(s, tiles));
+    const int64_t per = (n_ctx + s - 1) / s;
+    return ((per + kTT - 1) / kTT) * kTT;
+}
+
+}  // namespace
+
+int attend_simt_splits(const PoolView& p, int rows, int64_t n_ctx) {
+    const int64_t len = split_length(p, rows, n_ctx);
+    return (int)((n_ctx + len - 1) / len);
+}
+
+size_t attend_simt_workspace(const PoolView& p, int rows, int64_t n_ctx) {
+    const size_t S = (size_t)attend_simt_splits(p, rows, n_ctx);
+    const size_t U = (size_t)p.L * p.H;
+    return sizeof(float) * U * S * (size_t)rows * ((size_t)p.d + 2);
+}
+
+polykv_status launch_attend_simt(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
+                                 int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+    const int R = n_agents * (n_q_heads / p.H);
+    const int64_t len = split_length(p, R, n_ctx);
+    const int S = (int)((n_ctx + len - 1) / len);
+    if (ws_bytes < attend_simt_workspace(p, R, n_ctx))
+        return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend: workspace %zu < %zu bytes", ws_bytes,
+                         attend_simt_workspace(p, R, n_ctx));
+    float* w = static_cast<float*>(ws);
+    const bool bf = dt == POLYKV_BF16;
+    if (p.d == 128)
+        return bf ? dispatch_rows<128, true>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream)
+                  : dispatch_rows<128, false>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream);
+    if (p.d == 64)
+        return bf ? dispatch_rows<64, true>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream)
+                  : dispatch_rows<64, false>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream);
+    return set_error(POLYKV_E_UNSUPPORTED, "attend: head_dim %d", p.d);
+}
+
+}  // namespace polykv

@@ -1,0 +1,187 @@
+// C ABI of libpolykv: argument validation, pool layout, dispatch to kernels.
+// Host code only. The operations are those of "PolyKV: A Shared
+// Asymmetrically-Compressed KV Cache Pool for Multi-Agent LLM Inference"
+// (abstract): write one compressed pool once, let N agents attend over it.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "polykv_internal.cuh"
+
+struct polykv_pool {
+    polykv_pool_desc desc;
+    polykv::PoolView view;
+    polykv_pool_regions regions;
+    int64_t encoded;  // tokens [0, encoded) hold encoded data (as issued)
+};
+
+namespace polykv {
+
+static thread_local char g_err[512] = "";
+
+polykv_status set_error(polykv_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static polykv_status compute_regions(const polykv_pool_desc* d, polykv_pool_regions* r) {
+    if (!d) return set_error(POLYKV_E_INVAL, "desc is NULL");
+    if (d->n_layers <= 0 || d->n_kv_heads <= 0 || d->capacity_tokens <= 0)
+        return set_error(POLYKV_E_INVAL, "n_layers, n_kv_heads and capacity_tokens must be positive");
+    if (d->in_dtype != POLYKV_F16 && d->in_dtype != POLYKV_BF16)
+        return set_error(POLYKV_E_INVAL, "in_dtype must be POLYKV_F16 or POLYKV_BF16");
+    if (d->head_dim != 64 && d->head_dim != 128)
+        return set_error(POLYKV_E_UNSUPPORTED, "head_dim %d (supported: 64, 128)", d->head_dim);
+    if (d->capacity_tokens > ((int64_t)1 << 40)) return set_error(POLYKV_E_INVAL, "capacity_tokens too large");
+    const int64_t cap = (d->capacity_tokens + kTokenAlign - 1) / kTokenAlign * kTokenAlign;
+    const size_t units = (size_t)d->n_layers * (size_t)d->n_kv_heads;
+    const size_t hd = (size_t)d->head_dim;
+    const size_t toks = units * (size_t)cap;
+    size_t off = 0;
+    r->capacity_rounded = cap;
+    r->status_off = off;
+    off = align_up(off + 256, 256);
+    r->k_codes_off = off;
+    off = align_up(off + toks * hd, 256);
+    r->k_scales_off = off;
+    off = align_up(off + toks * (hd / kQ8Block) * 2, 256);
+    r->v_codes_off = off;
+    off = align_up(off + toks * (3 * hd / 8), 256);
+    r->v_norms_off = off;
+    off = align_up(off + toks * 2, 256);
+    r->total_bytes = off;
+    return POLYKV_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace polykv
+
+using namespace polykv;
+
+extern "C" {
+
+polykv_status polykv_pool_create(const polykv_pool_desc* desc, void* dev_buf, size_t dev_buf_bytes,
+                                 polykv_pool** out, size_t* required_bytes) {
+    polykv_pool_regions r;
+    const polykv_status st = compute_regions(desc, &r);
+    if (st != POLYKV_OK) return st;
+    if (required_bytes) *required_bytes = r.total_bytes;
+    if (!dev_buf) return POLYKV_OK;  // query mode
+    if (!out) return set_error(POLYKV_E_INVAL, "out is NULL");
+    if ((reinterpret_cast<uintptr_t>(dev_buf) & 255u) != 0)
+        return set_error(POLYKV_E_INVAL, "dev_buf must be 256-byte aligned");
+    if (dev_buf_bytes < r.total_bytes)
+        return set_error(POLYKV_E_BUFFER_TOO_SMALL, "dev_buf has %zu bytes, pool needs %zu", dev_buf_bytes,
+                         r.total_bytes);
+    polykv_pool* p = new (std::nothrow) polykv_pool;
+    if (!p) return set_error(POLYKV_E_INVAL, "host allocation failed");
+    p->desc = *desc;
+    p->regions = r;
+    p->encoded = 0;
+    char* base = static_cast<char*>(dev_buf);
+    p->view.kq = reinterpret_cast<int8_t*>(base + r.k_codes_off);
+    p->view.ks = reinterpret_cast<__half*>(base + r.k_scales_off);
+    p->view.vc = reinterpret_cast<uint8_t*>(base + r.v_codes_off);
+    p->view.vn = reinterpret_cast<__half*>(base + r.v_norms_off);
+    p->view.status = reinterpret_cast<uint32_t*>(base + r.status_off);
+    p->view.L = desc->n_layers;
+    p->view.H = desc->n_kv_heads;
+    p->view.d = desc->head_dim;
+    p->view.cap = r.capacity_rounded;
+    *out = p;
+    g_err[0] = 0;
+    return POLYKV_OK;
+}
+
+polykv_status polykv_pool_get_regions(const polykv_pool* pool, polykv_pool_regions* out) {
+    if (!pool || !out) return set_error(POLYKV_E_INVAL, "pool and out must be non-NULL");
+    *out = pool->regions;
+    return POLYKV_OK;
+}
+
+polykv_status polykv_encode(polykv_pool* pool, const void* k, const void* v, int64_t t0, int64_t n_tokens,
+                            void* stream) {
+    if (!pool) return set_error(POLYKV_E_INVAL, "pool is NULL");
+    if (n_tokens < 0 || t0 < 0) return set_error(POLYKV_E_INVAL, "t0 and n_tokens must be >= 0");
+    if (t0 + n_tokens > pool->desc.capacity_tokens)
+        return set_error(POLYKV_E_INVAL, "t0 + n_tokens = %lld exceeds capacity %lld", (long long)(t0 + n_tokens),
+                         (long long)pool->desc.capacity_tokens);
+    if (t0 > pool->encoded)
+        return set_error(POLYKV_E_STATE, "t0 = %lld leaves a gap after the %lld encoded tokens", (long long)t0,
+                         (long long)pool->encoded);
+    if (n_tokens == 0) return POLYKV_OK;
+    if (!k || !v) return set_error(POLYKV_E_INVAL, "k and v must be non-NULL");
+    if (!aligned16(k) || !aligned16(v)) return set_error(POLYKV_E_INVAL, "k and v must be 16-byte aligned");
+    const polykv_status st =
+        launch_encode(pool->view, pool->desc.in_dtype, k, v, t0, n_tokens, static_cast<cudaStream_t>(stream));
+    if (st != POLYKV_OK) return st;
+    if (t0 + n_tokens > pool->encoded) pool->encoded = t0 + n_tokens;
+    return POLYKV_OK;
+}
+
+static polykv_status check_attend_args(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads, int64_t n_ctx) {
+    if (!pool) return set_error(POLYKV_E_INVAL, "pool is NULL");
+    if (n_agents < 1) return set_error(POLYKV_E_INVAL, "n_agents must be >= 1");
+    if (n_q_heads < 1 || n_q_heads % pool->desc.n_kv_heads != 0)
+        return set_error(POLYKV_E_INVAL, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)", n_q_heads,
+                         pool->desc.n_kv_heads);
+    if (n_ctx < 1) return set_error(POLYKV_E_INVAL, "n_ctx must be >= 1");
+    if (n_ctx > pool->encoded)
+        return set_error(POLYKV_E_STATE, "n_ctx = %lld exceeds the %lld encoded tokens", (long long)n_ctx,
+                         (long long)pool->encoded);
+    if ((int64_t)n_agents * (n_q_heads / pool->desc.n_kv_heads) > (1 << 20))
+        return set_error(POLYKV_E_UNSUPPORTED, "too many query rows per kv head");
+    return POLYKV_OK;
+}
+
+polykv_status polykv_attend_workspace_size(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads,
+                                           int64_t n_ctx, size_t* bytes) {
+    const polykv_status st = check_attend_args(pool, n_agents, n_q_heads, n_ctx);
+    if (st != POLYKV_OK) return st;
+    if (!bytes) return set_error(POLYKV_E_INVAL, "bytes is NULL");
+    const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
+    *bytes = attend_simt_workspace(pool->view, rows, n_ctx);
+    return POLYKV_OK;
+}
+
+polykv_status polykv_attend(const polykv_pool* pool, const void* q, float* out, int32_t n_agents, int32_t n_q_heads,
+                            int64_t n_ctx, float softmax_scale, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    const polykv_status st = check_attend_args(pool, n_agents, n_q_heads, n_ctx);
+    if (st != POLYKV_OK) return st;
+    if (!q || !out) return set_error(POLYKV_E_INVAL, "q and out must be non-NULL");
+    if (!aligned16(q) || !aligned16(out) || (workspace && !aligned16(workspace)))
+        return set_error(POLYKV_E_INVAL, "q, out and workspace must be 16-byte aligned");
+    const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
+    const size_t need = attend_simt_workspace(pool->view, rows, n_ctx);
+    if (need > 0 && !workspace) return set_error(POLYKV_E_INVAL, "workspace is NULL but %zu bytes are needed", need);
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
+    return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
+                              workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+polykv_status polykv_free(polykv_pool* pool) {
+    delete pool;
+    return POLYKV_OK;
+}
+
+polykv_status polykv_codebook(float centroids[8], float boundaries[7]) {
+    if (centroids)
+        for (int i = 0; i < 8; ++i) centroids[i] = centroid_of(i);
+    if (boundaries) {
+        const float b[7] = {-kB6, -kB5, -kB4, 0.0f, kB4, kB5, kB6};
+        for (int i = 0; i < 7; ++i) boundaries[i] = b[i];
+    }
+    return POLYKV_OK;
+}
+
+const char* polykv_last_error(void) { return g_err; }
+
+}  // extern "C"

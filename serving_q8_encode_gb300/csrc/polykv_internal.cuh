@@ -1,0 +1,56 @@
+// Internal definitions shared by the libpolykv translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "polykv.h"
+
+namespace polykv {
+
+constexpr int kQ8Block = 32;       // q8_0 block length along head_dim
+constexpr int kTokenAlign = 128;   // pool capacity is rounded to this many tokens
+
+// 8-level Lloyd-Max quantizer for a unit Gaussian (Max 1960; the N(0,1)
+// codebook named in the PolyKV abstract), centroids rounded to fp32.
+constexpr float kC4 = 0.245094178944f;
+constexpr float kC5 = 0.756005281206f;
+constexpr float kC6 = 1.343909278505f;
+constexpr float kC7 = 2.151945704537f;
+// decision boundaries: midpoints formed in fp32 from the fp32 centroids
+constexpr float kB4 = (kC4 + kC5) * 0.5f;
+constexpr float kB5 = (kC5 + kC6) * 0.5f;
+constexpr float kB6 = (kC6 + kC7) * 0.5f;
+
+// Device view of a pool laid out in one caller buffer.
+struct PoolView {
+    int8_t* kq;        // [U][cap][d]
+    __half* ks;        // [U][cap][d/32]
+    uint8_t* vc;       // [U][cap][3d/8]
+    __half* vn;        // [U][cap]
+    uint32_t* status;  // small status block
+    int L, H, d;
+    int64_t cap;
+};
+
+polykv_status set_error(polykv_status st, const char* fmt, ...);
+
+polykv_status launch_encode(const PoolView& p, polykv_dtype dt, const void* k, const void* v, int64_t t0,
+                            int64_t n_tokens, cudaStream_t stream);
+
+// number of token splits used by the CUDA-core attention path
+int attend_simt_splits(const PoolView& p, int rows, int64_t n_ctx);
+size_t attend_simt_workspace(const PoolView& p, int rows, int64_t n_ctx);
+polykv_status launch_attend_simt(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
+                                 int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+__host__ __device__ inline float centroid_of(int code) {
+    // ascending codes 0..7 -> -c7 .. -c4, c4 .. c7
+    const float mag[4] = {kC4, kC5, kC6, kC7};
+    return code >= 4 ? mag[code - 4] : -mag[3 - code];
+}
+
+}  // namespace polykv

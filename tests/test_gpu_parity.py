@@ -1,0 +1,176 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on
+the same seeded inputs. Encode: q8 codes, scales, norms and 3-bit codes
+bit-exact (3-bit codes may differ only where the oracle's u lies within
+1e-6 * max(|b|, 1) of a boundary b, at most 1e-5 of elements). Attention:
+max abs error <= 2e-3 against the float64 oracle over the oracle's pool."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import serving_q8_encode_gb300 as pk
+    c32, b32 = oracle.codebook.codebook_f32()
+    return pk, torch, c32, b32
+
+
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def check_encode(pool, ref, n_tok, t_off=0, b32=None):
+    f = {k: v.cpu().numpy() for k, v in pool.fields().items()}
+    sl = slice(t_off, t_off + n_tok)
+    assert np.array_equal(f["k_codes"][:, :, sl], ref["k_codes"]), "q8 codes differ"
+    assert np.array_equal(f["k_scales"][:, :, sl].view(np.uint16), ref["k_scales"].view(np.uint16)), "scales differ"
+    assert np.array_equal(f["v_norms"][:, :, sl].view(np.uint16), ref["v_norms"].view(np.uint16)), "norms differ"
+    got = oracle.values.unpack_codes(f["v_packed"][:, :, sl], ref["v_codes"].shape[-1])
+    diff = got != ref["v_codes"]
+    if diff.any():
+        u = ref["u"][diff].astype(np.float64)
+        dist = np.min(np.abs(u[:, None] - b32.astype(np.float64)[None, :]) /
+                      np.maximum(np.abs(b32.astype(np.float64)), 1.0)[None, :], axis=1)
+        assert np.all(dist <= 1e-6), f"{int(diff.sum())} code mismatches away from a boundary"
+        assert diff.sum() <= max(1, 1e-5 * diff.size)
+    else:
+        assert np.array_equal(f["v_packed"][:, :, sl], ref["v_packed"])
+
+
+def run_case(env, L, H, Hq, d, T, A, dtype, seed=0, q_mult=1.0, n_ctx=None, layers=None, scale=0.0,
+             chunks=None):
+    pk, torch, c32, b32 = env
+    kb, vb = synth.gen_kv(L, H, T, d, dtype, seed)
+    qb = synth.gen_q(L, A, Hq, d, dtype, seed, q_mult=q_mult)
+    pool = pk.Pool(L, H, d, T, dtype)
+    if chunks is None:
+        pool.encode(_dev(torch, kb), _dev(torch, vb))
+    else:  # append in pieces
+        t0 = 0
+        for c in chunks:
+            pool.encode(_dev(torch, kb[:, :, t0:t0 + c]), _dev(torch, vb[:, :, t0:t0 + c]), t0=t0)
+            t0 += c
+    n_ctx = T if n_ctx is None else n_ctx
+    out = pool.attend(_dev(torch, qb), n_ctx, softmax_scale=scale)
+    torch.cuda.synchronize()
+    ref_pool = oracle.attention.encode_pool(kb, vb, dtype, b32)
+    check_encode(pool, ref_pool, T, 0, b32)
+    ref = oracle.attention.attend_pool(qb, dtype, ref_pool, n_ctx, c32,
+                                       scale=(scale if scale > 0 else None), layers=layers)
+    got = out.cpu().numpy().astype(np.float64)
+    if layers is not None:
+        got = got[list(layers)]
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got))
+    assert err.max() <= ATOL, f"max abs err {err.max():.3e} (rel {err.max() / np.abs(ref).max():.2e})"
+    return err.max()
+
+
+# ---- the pages' model shapes
+def test_smollm2_single_layer_600(env):
+    run_case(env, 1, 32, 32, 64, 600, 1, "f16")
+
+
+def test_smollm2_full_stack_1851_5_agents(env):
+    run_case(env, 24, 32, 32, 64, 1851, 5, "f16", layers=[0, 5, 11, 23])
+
+
+def test_llama3_8b_4096_15_agents_sampled_layers(env):
+    run_case(env, 32, 8, 32, 128, 4096, 15, "bf16", layers=[0, 13, 31])
+
+
+def test_llama3_8b_7194_context(env):
+    run_case(env, 2, 8, 32, 128, 7194, 15, "bf16")
+
+
+# ---- ragged and degenerate cases
+@pytest.mark.parametrize("T", [1, 31, 33, 64, 65, 129, 257])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_lengths(env, T, d):
+    run_case(env, 1, 2, 8, d, T, 3, "bf16" if d == 128 else "f16", seed=T)
+
+
+@pytest.mark.parametrize("A,G", [(1, 1), (2, 4), (15, 4), (20, 4), (33, 2), (7, 1)])
+def test_rows_per_kv_head(env, A, G):
+    run_case(env, 2, 2, 2 * G, 128, 200, A, "bf16", seed=A)
+
+
+def test_peaky_queries_online_rescale(env):
+    run_case(env, 2, 4, 16, 128, 1000, 4, "bf16", q_mult=8.0)
+
+
+def test_very_peaky_queries(env):
+    run_case(env, 1, 2, 8, 64, 700, 3, "f16", q_mult=40.0)
+
+
+def test_zero_queries_give_mean(env):
+    run_case(env, 1, 2, 8, 128, 300, 2, "bf16", q_mult=0.0)
+
+
+def test_custom_softmax_scale(env):
+    run_case(env, 1, 4, 4, 64, 150, 2, "f16", scale=0.37)
+
+
+def test_partial_context_and_append(env):
+    run_case(env, 2, 2, 8, 128, 500, 3, "bf16", n_ctx=333, chunks=[100, 1, 199, 200])
+
+
+def test_encode_overwrite_in_place(env):
+    pk, torch, c32, b32 = env
+    L, H, d, T = 1, 2, 128, 64
+    k1, v1 = synth.gen_kv(L, H, T, d, "bf16", 1)
+    k2, v2 = synth.gen_kv(L, H, 16, d, "bf16", 2)
+    pool = pk.Pool(L, H, d, T, "bf16")
+    pool.encode(_dev(torch, k1), _dev(torch, v1))
+    pool.encode(_dev(torch, k2), _dev(torch, v2), t0=10)
+    torch.cuda.synchronize()
+    k = k1.copy()
+    v = v1.copy()
+    k[:, :, 10:26] = k2
+    v[:, :, 10:26] = v2
+    check_encode(pool, oracle.attention.encode_pool(k, v, "bf16", b32), T, 0, b32)
+
+
+def test_zero_value_vectors_and_constant_keys(env):
+    pk, torch, c32, b32 = env
+    L, H, d, T = 1, 1, 64, 40
+    kb = np.zeros((L, H, T, d), np.uint16)
+    vb = np.zeros((L, H, T, d), np.uint16)
+    kb[..., 5:9, :] = synth.f32_to_f16_bits(np.full((1, 1, 4, d), 0.5, np.float32))
+    pool = pk.Pool(L, H, d, T, "f16")
+    pool.encode(_dev(torch, kb), _dev(torch, vb))
+    qb = synth.gen_q(L, 2, 2, d, "f16", 3)
+    out = pool.attend(_dev(torch, qb), T)
+    torch.cuda.synchronize()
+    check_encode(pool, oracle.attention.encode_pool(kb, vb, "f16", b32), T, 0, b32)
+    assert np.all(out.cpu().numpy() == 0.0)
+
+
+def test_two_pools_interleaved_streams(env):
+    pk, torch, c32, b32 = env
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    L, H, Hq, d, T, A = 1, 4, 16, 128, 300, 2
+    kb, vb = synth.gen_kv(L, H, T, d, "bf16", 9)
+    qb = synth.gen_q(L, A, Hq, d, "bf16", 9)
+    pool = pk.Pool(L, H, d, T, "bf16")
+    pool.encode(_dev(torch, kb), _dev(torch, vb))
+    torch.cuda.synchronize()
+    q = _dev(torch, qb)
+    ws1 = torch.empty(pool.workspace_size(A, Hq, T), dtype=torch.uint8, device="cuda")
+    ws2 = torch.empty_like(ws1)
+    with torch.cuda.stream(s1):
+        o1 = pool.attend(q, T, workspace=ws1, stream=s1)
+    with torch.cuda.stream(s2):
+        o2 = pool.attend(q, T, workspace=ws2, stream=s2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
