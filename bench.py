@@ -262,7 +262,7 @@ def run_polykv(args, w: synth.Workload):
     hq = torch.from_numpy(qb.view(np.int16)).pin_memory()
     hout = torch.empty((L, A, Hq, d), dtype=torch.float32).pin_memory()
     e2e_ms = []
-    for i in range(max(2, args.steps // 2) + 1):
+    for i in range(0 if args.no_e2e else max(2, args.steps // 2) + 1):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         k.copy_(hk, non_blocking=True)
@@ -274,7 +274,7 @@ def run_polykv(args, w: synth.Workload):
         torch.cuda.synchronize()
         if i > 0:
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e_ms_m = float(np.mean(e2e_ms))
+    e2e_ms_m = float(np.mean(e2e_ms)) if e2e_ms else float("nan")
 
     def allmax(x):
         if world == 1:
@@ -340,8 +340,14 @@ def main():
     ap.add_argument("--impl", default="polykv", choices=["polykv", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the layer count (smaller cases for profiler captures)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.layers is not None:
+        import dataclasses
+        w = dataclasses.replace(w, n_layers=args.layers, name=f"{w.name}_L{args.layers}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_polykv(args, w)
