@@ -77,7 +77,9 @@ typedef struct {
     size_t k_scales_off;
     size_t v_codes_off;
     size_t v_norms_off;
-    size_t status_off;        /* small device status block used by the kernels */
+    size_t status_off;        /* uint32 status word (see polykv_pool_status) */
+    size_t v_nmax_off;        /* float [U]: running max of ||v|| per unit (kept by encode) */
+    size_t header_bytes;      /* [status_off, header_bytes) is cleared by the first encode */
     size_t total_bytes;
 } polykv_pool_regions;
 
@@ -94,7 +96,8 @@ typedef struct {
  *                   release with polykv_free). May be NULL in query mode.
  *   required_bytes  receives the bytes the pool needs (may be NULL when
  *                   dev_buf is not NULL).
- * Enqueues no device work; the pool's contents are undefined until encoded.
+ * Enqueues no device work; the pool's contents are undefined until encoded
+ * (the first polykv_encode clears the pool header on its stream).
  * Errors: E_INVAL (null desc, non-positive sizes, misaligned dev_buf),
  * E_UNSUPPORTED (head_dim not 64/128), E_BUFFER_TOO_SMALL. */
 POLYKV_API polykv_status polykv_pool_create(const polykv_pool_desc* desc, void* dev_buf, size_t dev_buf_bytes,
@@ -117,6 +120,9 @@ POLYKV_API polykv_status polykv_pool_get_regions(const polykv_pool* pool, polykv
  *   n_tokens  >= 0; t0 + n_tokens <= capacity_tokens. 0 is a no-op.
  * One kernel launch on `stream`. Ordering against attend calls on the same
  * pool is the caller's job (same stream or events): one writer, then readers.
+ * The encode also raises the per-unit maximum of ||v|| kept in the pool header
+ * (attention uses it to scale fp16 operands); the first encode into a pool
+ * clears that header first (a cudaMemsetAsync on `stream`).
  * Errors: E_INVAL, E_STATE (t0 beyond the encoded prefix), E_CUDA. */
 POLYKV_API polykv_status polykv_encode(polykv_pool* pool, const void* k, const void* v, int64_t t0, int64_t n_tokens,
                             void* stream);
@@ -145,6 +151,13 @@ POLYKV_API polykv_status polykv_attend_workspace_size(const polykv_pool* pool, i
 POLYKV_API polykv_status polykv_attend(const polykv_pool* pool, const void* q, float* out, int32_t n_agents,
                             int32_t n_q_heads, int64_t n_ctx, float softmax_scale, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* Read and clear the pool's device status word (synchronises `stream`).
+ * Bit 0: a kernel gave up on a bounded device-side wait (about 2 s) and its
+ * results are invalid; the call then returns POLYKV_E_TIMEOUT. *flags gets the
+ * raw word. The word is cleared by the first encode into the pool.
+ * Errors: E_INVAL, E_CUDA, E_TIMEOUT. */
+POLYKV_API polykv_status polykv_pool_status(const polykv_pool* pool, void* stream, uint32_t* flags);
 
 /* Release a handle (host memory only; dev_buf stays the caller's). NULL is OK. */
 POLYKV_API polykv_status polykv_free(polykv_pool* pool);

@@ -38,7 +38,8 @@ class PoolDesc(ctypes.Structure):
 class PoolRegions(ctypes.Structure):
     _fields_ = [("capacity_rounded", ctypes.c_int64), ("k_codes_off", ctypes.c_size_t),
                 ("k_scales_off", ctypes.c_size_t), ("v_codes_off", ctypes.c_size_t),
-                ("v_norms_off", ctypes.c_size_t), ("status_off", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
+                ("v_norms_off", ctypes.c_size_t), ("status_off", ctypes.c_size_t), ("v_nmax_off", ctypes.c_size_t),
+                ("header_bytes", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -62,6 +63,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "polykv_attend": [vp, vp, vp, i32, i32, i64, f32, vp, sz, vp],
         "polykv_free": [vp],
         "polykv_codebook": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
+        "polykv_pool_status": [vp, vp, ctypes.POINTER(ctypes.c_uint32)],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -109,6 +111,13 @@ def polykv_attend(handle: int, q_ptr: int, out_ptr: int, n_agents: int, n_q_head
                   softmax_scale: float, ws_ptr: int | None, ws_bytes: int, stream: int | None):
     _check(load_library().polykv_attend(handle, q_ptr, out_ptr, n_agents, n_q_heads, n_ctx, softmax_scale, ws_ptr,
                                         ws_bytes, stream))
+
+
+def polykv_pool_status(handle: int, stream: int | None) -> int:
+    """Reads and clears the pool's device status word; raises PolyKVError(E_TIMEOUT) if a kernel gave up."""
+    f = ctypes.c_uint32()
+    _check(load_library().polykv_pool_status(handle, stream, ctypes.byref(f)))
+    return f.value
 
 
 def polykv_free(handle: int | None):
@@ -166,6 +175,9 @@ class Pool:
         L, H, n, d = k.shape
         assert (L, H, d) == (self.desc.n_layers, self.desc.n_kv_heads, self.desc.head_dim)
         polykv_encode(self.handle, k.data_ptr(), v.data_ptr(), t0, n, _stream_handle(stream))
+
+    def status(self, stream=None) -> int:
+        return polykv_pool_status(self.handle, _stream_handle(stream))
 
     def workspace_size(self, n_agents: int, n_q_heads: int, n_ctx: int) -> int:
         return polykv_attend_workspace_size(self.handle, n_agents, n_q_heads, n_ctx)

@@ -266,10 +266,14 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
 
 // One warp per (unit, row): log-sum-exp merge of the splits, normalisation,
 // one inverse FWHT of the row (o = (1/d) H acc / l), fp32 output.
+// Partials of unit u live in slots u*n_slots + k. With nc > 0 the slots come
+// from a contiguous cut of the (unit, tile) list into nc ranges (tt tiles,
+// nt per unit) and unit u has one piece per range that overlaps it;
+// otherwise every unit has n_slots pieces.
 template <int D>
 __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
                                                     float* __restrict__ out, int U, int H, int A, int Hq, int R,
-                                                    int n_splits) {
+                                                    int n_slots, int64_t nt, int64_t tt, int nc) {
     constexpr int EPL = D / 32;  // elements per lane
     const int wid = blockIdx.x * 4 + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -279,14 +283,20 @@ __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws
     const int layer = unit / H, kvh = unit % H;
     const int a = r / G, g = r % G;
 
+    int pieces = n_slots;
+    if (nc > 0) {
+        const int64_t lo = (((int64_t)unit * nt + 1) * nc - 1) / tt;
+        const int64_t hi = (((int64_t)unit * nt + nt) * nc - 1) / tt;
+        pieces = (int)(hi - lo + 1);
+    }
     float M = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[(((int64_t)unit * n_splits + s) * R + r) * 2]);
+    for (int s = 0; s < pieces; ++s) M = fmaxf(M, ws_ml[(((int64_t)unit * n_slots + s) * R + r) * 2]);
     float L = 0.0f;
     float o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
-    for (int s = 0; s < n_splits; ++s) {
-        const int64_t pr = ((int64_t)unit * n_splits + s) * R + r;
+    for (int s = 0; s < pieces; ++s) {
+        const int64_t pr = ((int64_t)unit * n_slots + s) * R + r;
         const float ms = ws_ml[pr * 2];
         if (ms == -INFINITY) continue;
         const float w = exp2f(ms - M);
@@ -337,11 +347,7 @@ polykv_status run_simt(const PoolView& p, const void* q, float* out, int A, int 
                                             scale * kLog2e, ws_acc, ws_ml);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend partial launch: %s", cudaGetErrorString(e));
-    const int warps = U * R;
-    attend_merge<D><<<(warps + 3) / 4, 128, 0, st>>>(ws_acc, ws_ml, out, U, p.H, A, Hq, R, n_splits);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend merge launch: %s", cudaGetErrorString(e));
-    return POLYKV_OK;
+    return launch_attend_merge(ws_acc, ws_ml, out, U, p.H, A, Hq, R, n_splits, 0, 0, 0, D, st);
 }
 
 template <int D, bool BF16>
@@ -365,6 +371,19 @@ int64_t split_length(const PoolView& p, int rows, int64_t n_ctx) {
 }
 
 }  // namespace
+
+polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float* out, int U, int H, int A, int Hq,
+                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st) {
+    const int64_t warps = (int64_t)U * R;
+    const unsigned blocks = (unsigned)((warps + 3) / 4);
+    if (D == 128)
+        attend_merge<128><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc);
+    else
+        attend_merge<64><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend merge launch: %s", cudaGetErrorString(e));
+    return POLYKV_OK;
+}
 
 int attend_simt_splits(const PoolView& p, int rows, int64_t n_ctx) {
     const int64_t len = split_length(p, rows, n_ctx);

@@ -1,0 +1,710 @@
+// Multi-agent decode attention over the shared pool on the 5th-generation
+// tensor cores (tcgen05, TMEM accumulators), head_dim 128, up to 64 query
+// rows per kv head (agents x GQA group).
+//
+// PolyKV abstract ("PolyKV: A Shared Asymmetrically-Compressed KV Cache Pool
+// for Multi-Agent LLM Inference"): N agents read one compressed pool. With 15
+// agents x 4 GQA heads = 60 rows per kv head, q.K and p.V are dense
+// contractions (about 156 flop per pool byte), so both run as tcgen05.mma:
+//
+//   MMA1 (per 128-token tile, per 32-wide q8_0 block b):
+//        S_b^T[token][row] = K_b[token][32] . Q_b[row][32]^T
+//        A = int8 key codes converted exactly to fp16 and written to TMEM by
+//        the producer warps; B = the rows' queries in fp16, scaled by a power of
+//        two (bf16 queries are then represented exactly); four fp32
+//        accumulators so each block's fp16 scale multiplies its own partial
+//        sum, as in the q8_0 definition.
+//   softmax (one thread per token and row group; TMEM lane = token):
+//        x = sum_b s_b * S_b (base-2 logits), online max with lazy rescaling
+//        (only when a logit exceeds the running max by more than 2^6),
+//        p = 2^(x - m), P' = p * ||v|| * w in fp16, w a power of two from the
+//        pool's per-unit norm maximum (so P' < 2^14).
+//   MMA2: O^T[dim][row] += Vc[token][dim]^T . P'[token][row], A = the 3-bit
+//        value codes expanded to fp16 centroids in the ROTATED basis; the
+//        inverse FWHT is applied once per output row by the merge kernel.
+//
+// Data movement: one TMA thread streams each 128-token tile of the pool
+// (key codes as a 128B-swizzled 2-D tile, scales / value codes / norms as
+// 1-D bulk copies) into a 4-deep shared-memory ring, so about 95 KB per SM
+// are in flight; every pool byte is read from HBM once for all agents.
+// Work: the (layer, kv head, tile) list is cut into one contiguous range per
+// CTA (one persistent CTA per SM); a range that crosses a unit boundary
+// writes one softmax partial per unit piece; the merge kernel combines them.
+//
+// Warp roles (448 threads): 0-3 producers (key codes -> TMEM, value codes ->
+// centroids in shared memory), 4-11 softmax in two row groups of 32, 12 MMA
+// issue + TMEM owner, 13 TMA. Every mbarrier wait is bounded (2 s); on expiry
+// the CTA raises an abort flag, skips the rest of its work, waits (bounded)
+// for its copies in flight, frees its TMEM and sets the pool's status word.
+#include <cmath>
+#include <cuda.h>
+
+#include "polykv_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace polykv {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kD = 128;
+constexpr int kNR = 64;            // padded rows (MMA N)
+constexpr int kThreadsTc = 448;
+constexpr int kNS = 4;             // pool-tile ring depth
+constexpr float kTau = 6.0f;       // lazy rescale threshold (log2 units)
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr float kLog2eTc = 1.4426950408889634f;
+
+// one ring stage: key codes (swizzled) | scales | value codes | norms
+constexpr uint32_t kRawK = 0, kRawS = 16384, kRawV = 17408, kRawN = 23552;
+constexpr uint32_t kRawBytes = 23808;      // bytes delivered per tile
+constexpr uint32_t kRawStage = 24576;      // stage stride (keeps key tiles 1024-aligned)
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t kSmQ = 0;                            // 2 chunks x [64 rows][128 B]          16 KB
+constexpr uint32_t kSmV = kSmQ + 16384;                 // 2 stages x 2 dim blocks x [128][128 B] 64 KB
+constexpr uint32_t kSmP = kSmV + 65536;                 // 2 stages x [128 tokens][128 B]       32 KB
+constexpr uint32_t kSmRaw = kSmP + 32768;               // kNS x 24 KB                          96 KB
+constexpr uint32_t kSmLut = kSmRaw + kNS * kRawStage;   // 64 code pairs x 32 lanes x 4 B         8 KB
+constexpr uint32_t kSmMisc = kSmLut + 8192;
+constexpr uint32_t kSmBytes = kSmMisc + 2048 + 1024;    // + alignment slack
+static_assert(kSmBytes <= 232448, "shared memory budget");
+
+// TMEM columns
+constexpr uint32_t kColK = 0;     // 2 stages x 64
+constexpr uint32_t kColS = 128;   // 4 blocks x 64
+constexpr uint32_t kColO = 384;   // 64
+constexpr uint32_t kTmemCols = 512;
+
+struct TcParams {
+    PoolView p;
+    const uint16_t* q;
+    float* ws_acc;
+    float* ws_ml;
+    int64_t n_ctx;
+    int64_t total_tiles;
+    int A, Hq, G, R;
+    int nt;      // tiles per unit
+    int nctas;
+    int pmax;    // partial slots per unit
+    float scale_log2;
+};
+
+struct Misc {
+    float msm[kNR];       // running max per row (log2 units)
+    float alpha[kNR];
+    float red[2][4][32];
+    float qred[8];
+    float scale_eff;
+    float wscale;
+    int flags[2][3];
+    int abort;
+    int pad;
+    uint64_t kfull[2], kfree[2], vfull[2], pfull[2], pvfree[2], sfull, sfree, qready;
+    uint64_t rfull[kNS], rempty[kNS];
+    uint32_t tslot;
+};
+static_assert(sizeof(Misc) <= 2048, "misc block");
+
+__device__ __forceinline__ int64_t cta_of_tile(int64_t g, int64_t tt, int nc) { return ((g + 1) * nc - 1) / tt; }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// int8 x4 -> two fp16x2 words, exactly: fp16(0x6400 | (x ^ 0x80)) = 1024 + x + 128.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t magic = 0x64646464u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(magic));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(magic));
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+template <int K>
+__device__ __forceinline__ uint32_t code_pair(const uint32_t (&w)[12]) {
+    // 6-bit field (two consecutive 3-bit codes) at bit 6K of the 384-bit row
+    constexpr int bit = 6 * K, word = bit >> 5, off = bit & 31;
+    if constexpr (off <= 26) {
+        return (w[word] >> off) & 63u;
+    } else {
+        return ((w[word] >> off) | (w[word + 1] << (32 - off))) & 63u;
+    }
+}
+
+template <int C>
+__device__ __forceinline__ void store_v_chunks(const uint32_t (&w)[12], const uint32_t* lut, uint8_t* vstage,
+                                               uint32_t tok, bool valid) {
+    if constexpr (C < 16) {
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+            o.x = lut[code_pair<4 * C + 0>(w) * 32];
+            o.y = lut[code_pair<4 * C + 1>(w) * 32];
+            o.z = lut[code_pair<4 * C + 2>(w) * 32];
+            o.w = lut[code_pair<4 * C + 3>(w) * 32];
+        }
+        // dims 8C..8C+7 -> dim block C/8, chunk C%8 of this token's 128-byte row
+        *reinterpret_cast<uint4*>(vstage + (C / 8) * 16384 + tc::sw128(tok, (C % 8) * 16)) = o;
+        store_v_chunks<C + 1>(w, lut, vstage, tok, valid);
+    }
+}
+
+template <bool QBF16>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u = tc::smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
+    uint8_t* sQ = sm + kSmQ;
+    uint8_t* sV = sm + kSmV;
+    uint8_t* sP = sm + kSmP;
+    uint8_t* sR = sm + kSmRaw;
+    uint32_t* lut = reinterpret_cast<uint32_t*>(sm + kSmLut);
+    Misc& M = *reinterpret_cast<Misc*>(sm + kSmMisc);
+    volatile int* abortp = &M.abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t TT = P.total_tiles;
+    const int c = blockIdx.x;
+    const int64_t g0 = (int64_t)c * TT / P.nctas;
+    const int64_t g1 = (int64_t)(c + 1) * TT / P.nctas;
+    const int64_t n = g1 - g0;
+    const int nt = P.nt;
+    const int64_t cap = P.p.cap;
+
+    // ---- set-up: barriers, codebook pairs, TMEM
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(tc::smem_u32(&M.kfull[s]), 128);
+            tc::mbar_init(tc::smem_u32(&M.kfree[s]), 1);
+            tc::mbar_init(tc::smem_u32(&M.vfull[s]), 128);
+            tc::mbar_init(tc::smem_u32(&M.pfull[s]), 256);
+            tc::mbar_init(tc::smem_u32(&M.pvfree[s]), 1);
+        }
+        for (int s = 0; s < kNS; ++s) {
+            tc::mbar_init(tc::smem_u32(&M.rfull[s]), 1);
+            tc::mbar_init(tc::smem_u32(&M.rempty[s]), 128 + 256);
+        }
+        tc::mbar_init(tc::smem_u32(&M.sfull), 1);
+        tc::mbar_init(tc::smem_u32(&M.sfree), 256);
+        tc::mbar_init(tc::smem_u32(&M.qready), 1);
+        M.abort = 0;
+        for (int g = 0; g < 2; ++g) M.flags[g][0] = M.flags[g][1] = M.flags[g][2] = 0;
+        tc::mbar_init_fence();
+    }
+    for (int e = tid; e < 64 * 32; e += kThreadsTc) {
+        const int idx = e >> 5;
+        const __half lo = __float2half_rn(centroid_of(idx & 7));
+        const __half hi = __float2half_rn(centroid_of(idx >> 3));
+        lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    }
+    if (warp == 12) tc::tmem_alloc(tc::smem_u32(&M.tslot), kTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tbase = M.tslot;
+
+    if (warp == 13) {
+        // =============================== TMA: pool tiles into the ring
+        if (lane == 0) {
+            int64_t issued = 0;
+            for (int64_t j = 0; j < n; ++j) {
+                const int st = (int)(j % kNS);
+                if (j >= kNS &&
+                    !tc::mbar_wait(tc::smem_u32(&M.rempty[st]), (uint32_t)(((j / kNS) - 1) & 1), abortp, kTimeoutNs))
+                    break;
+                const int64_t g = g0 + j;
+                const int64_t u = g / nt;
+                const int64_t row0 = u * cap + (g - u * nt) * kTile;
+                const uint32_t dst = tc::smem_u32(sR + st * kRawStage);
+                const uint32_t bar = tc::smem_u32(&M.rfull[st]);
+                tc::mbar_arrive_expect_tx(bar, kRawBytes);
+                tc::tma_2d_g2s(dst + kRawK, &kmap, 0, (int32_t)row0, bar);
+                tc::bulk_g2s(dst + kRawS, P.p.ks + row0 * (kD / kQ8Block), 1024, bar);
+                tc::bulk_g2s(dst + kRawV, P.p.vc + row0 * (3 * kD / 8), 6144, bar);
+                tc::bulk_g2s(dst + kRawN, P.p.vn + row0, 256, bar);
+                issued = j + 1;
+            }
+            // drain: never leave copies in flight into shared memory that is about to be released
+            for (int64_t j = issued > kNS ? issued - kNS : 0; j < issued; ++j) {
+                volatile int dummy = 0;
+                tc::mbar_wait(tc::smem_u32(&M.rfull[j % kNS]), (uint32_t)((j / kNS) & 1), &dummy, 50000000ull);
+            }
+        }
+    } else if (warp < 4) {
+        // =============================== producers
+        const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t = (uint32_t)tid;
+        for (int64_t j = 0; j < n && !*abortp; ++j) {
+            const int64_t g = g0 + j;
+            const int64_t u = g / nt;
+            const int64_t ti = g - u * nt;
+            const int s = (int)(j & 1);
+            const uint32_t ph = (uint32_t)((j >> 1) & 1);
+            const int st = (int)(j % kNS);
+            const bool valid = ti * kTile + t < P.n_ctx;
+            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
+            const uint8_t* raw = sR + st * kRawStage;
+            // keys: int8 codes -> fp16 -> TMEM lane = token
+            if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.kfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                uint32_t r[16];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint4 kr = make_uint4(0u, 0u, 0u, 0u);
+                    if (valid) kr = *reinterpret_cast<const uint4*>(raw + kRawK + tc::sw128(t, (2 * qq + h) * 16));
+                    i8x4_to_f16x4(kr.x, r[h * 8 + 0], r[h * 8 + 1]);
+                    i8x4_to_f16x4(kr.y, r[h * 8 + 2], r[h * 8 + 3]);
+                    i8x4_to_f16x4(kr.z, r[h * 8 + 4], r[h * 8 + 5]);
+                    i8x4_to_f16x4(kr.w, r[h * 8 + 6], r[h * 8 + 7]);
+                }
+                tc::tmem_st16(lane_addr + kColK + 64u * s + 16u * qq, r);
+            }
+            tc::wait_st();
+            tc::fence_before();
+            tc::mbar_arrive(tc::smem_u32(&M.kfull[s]));
+            // values: packed 3-bit codes -> fp16 centroids, token-major rows (MN-major A operand)
+            if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
+            uint32_t w[12];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const uint4 x = *reinterpret_cast<const uint4*>(raw + kRawV + t * 48 + 16 * i);
+                w[4 * i] = x.x;
+                w[4 * i + 1] = x.y;
+                w[4 * i + 2] = x.z;
+                w[4 * i + 3] = x.w;
+            }
+            tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
+            store_v_chunks<0>(w, lut + lane, sV + s * 32768, t, valid);
+            tc::fence_proxy_async();
+            tc::mbar_arrive(tc::smem_u32(&M.vfull[s]));
+        }
+    } else if (warp < 12) {
+        // =============================== softmax + epilogue (two groups of 32 rows)
+        const int grp = (warp - 4) >> 2;        // row group: rows 32*grp .. 32*grp+31
+        const int wq = warp & 3;                // TMEM lane quadrant
+        const int tt = wq * 32 + lane;          // token slot = TMEM lane (= head-dim index in the epilogue)
+        const int si = tid - 128;               // 0..255 over both groups
+        const uint32_t lane_addr = tbase + ((uint32_t)(wq * 32) << 16);
+        const uint32_t gbar = 1 + grp;
+        const int R = P.R;
+        const int rbase = 32 * grp;
+        int seg = -1;
+        int64_t seg_u = -1;
+        float ls[32];
+        for (int64_t j = 0; j < n; ++j) {
+            const int64_t g = g0 + j;
+            const int64_t u = g / nt;
+            const int64_t ti = g - u * nt;
+            const int s = (int)(j & 1);
+            const uint32_t ph = (uint32_t)((j >> 1) & 1);
+            const int st = (int)(j % kNS);
+            const bool first = (j == 0) || (ti == 0);
+            const bool last = (j == n - 1) || (ti == nt - 1);
+            if (first) {
+                // -------- segment prologue (both groups): queries, operand scales, row state
+                ++seg;
+                seg_u = u;
+                const int layer = (int)(u / P.p.H), kvh = (int)(u % P.p.H);
+                uint4 qv[4];
+                float qm = 0.0f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int cid = si + 256 * m;
+                    qv[m] = make_uint4(0u, 0u, 0u, 0u);
+                    if (cid < R * 16) {
+                        const int r = cid >> 4, dc = cid & 15;
+                        const int a = r / P.G, gq = r % P.G;
+                        qv[m] = __ldg(reinterpret_cast<const uint4*>(
+                                          P.q + (((int64_t)layer * P.A + a) * P.Hq + kvh * P.G + gq) * kD) + dc);
+                        const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float lo, hi;
+                            if (QBF16) {
+                                lo = __uint_as_float(wv[e] << 16);
+                                hi = __uint_as_float(wv[e] & 0xFFFF0000u);
+                            } else {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+                                lo = f.x;
+                                hi = f.y;
+                            }
+                            qm = fmaxf(qm, fmaxf(fabsf(lo), fabsf(hi)));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+                if (lane == 0) M.qred[warp - 4] = qm;
+                tc::named_bar(3, 256);
+                float qmax = 0.0f;
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) qmax = fmaxf(qmax, M.qred[w8]);
+                int eq = 0;
+                if (qmax > 0.0f) frexpf(qmax, &eq);
+                const float fq = qmax > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;  // qmax * fq in [2^14, 2^15)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int cid = si + 256 * m;
+                    if (cid < kNR * 16) {
+                        const int r = cid >> 4, dc = cid & 15;
+                        const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+                        uint32_t hv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float lo = 0.0f, hi = 0.0f;
+                            if (r < R) {
+                                if (QBF16) {
+                                    lo = __uint_as_float(wv[e] << 16);
+                                    hi = __uint_as_float(wv[e] & 0xFFFF0000u);
+                                } else {
+                                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+                                    lo = f.x;
+                                    hi = f.y;
+                                }
+                            }
+                            const __half2 h = __floats2half2_rn(lo * fq, hi * fq);
+                            hv[e] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        *reinterpret_cast<uint4*>(sQ + (dc >> 3) * 8192 + tc::sw128(r, (dc & 7) * 16)) =
+                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    }
+                }
+                if (si == 0) {
+                    const float nmax = P.p.nmax[u];
+                    int en = 0;
+                    if (nmax > 0.0f) frexpf(nmax, &en);
+                    M.scale_eff = P.scale_log2 / fq;
+                    M.wscale = nmax > 0.0f ? ldexpf(1.0f, 8 - en) : 1.0f;  // ||v|| * wscale < 2^8
+                }
+                if (si < kNR) M.msm[si] = -INFINITY;
+                tc::fence_proxy_async();
+                tc::named_bar(3, 256);
+                if (si == 0) tc::mbar_arrive(tc::smem_u32(&M.qready));
+#pragma unroll
+                for (int k = 0; k < 32; ++k) ls[k] = 0.0f;
+            }
+            const float scale_eff = M.scale_eff;
+            const float wscale = M.wscale;
+            const int64_t tok = ti * kTile + tt;
+            const bool valid = tok < P.n_ctx;
+            // per-token block scales and norm from the ring
+            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
+            const uint8_t* raw = sR + st * kRawStage;
+            const uint2 sr = *reinterpret_cast<const uint2*>(raw + kRawS + tt * 8);
+            const unsigned short nb = *reinterpret_cast<const unsigned short*>(raw + kRawN + tt * 2);
+            tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
+            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sr.x));
+            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sr.y));
+            const float sb[4] = {s01.x * scale_eff, s01.y * scale_eff, s23.x * scale_eff, s23.y * scale_eff};
+            const float wt = valid ? __half2float(__ushort_as_half(nb)) * wscale : 0.0f;
+            // -------- logits from the four block accumulators (this group's 32 rows)
+            float x[32];
+            tc::mbar_wait(tc::smem_u32(&M.sfull), (uint32_t)(j & 1), abortp, kTimeoutNs);
+            tc::fence_after();
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                uint32_t t0[16], t1[16];
+                tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 0u, t0);
+                tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 16u, t1);
+                tc::wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    if (b == 0) {
+                        x[k] = sb[0] * __uint_as_float(t0[k]);
+                        x[16 + k] = sb[0] * __uint_as_float(t1[k]);
+                    } else {
+                        x[k] = fmaf(sb[b], __uint_as_float(t0[k]), x[k]);
+                        x[16 + k] = fmaf(sb[b], __uint_as_float(t1[k]), x[16 + k]);
+                    }
+                }
+            }
+            tc::fence_before();
+            tc::mbar_arrive(tc::smem_u32(&M.sfree));
+            if (!valid) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) x[k] = -INFINITY;
+            }
+            // -------- lazy rescale decision (per row group)
+            bool need = false;
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (rbase + k < R) need |= (x[k] - M.msm[rbase + k] > kTau);
+            if (tt == 0) M.flags[grp][(j + 1) % 3] = 0;
+            if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&M.flags[grp][j % 3], 1);
+            tc::named_bar(gbar, 128);
+            if (M.flags[grp][j % 3]) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    float v = x[k];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    if (lane == k) M.red[grp][wq][k] = v;
+                }
+                tc::named_bar(gbar, 128);
+                if (tt < 32) {
+                    const int r = rbase + tt;
+                    const float mo = M.msm[r];
+                    const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
+                                           fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
+                    const float mn = fmaxf(mo, mt);
+                    M.alpha[r] = (mo == -INFINITY || mn == -INFINITY) ? 0.0f : ex2(mo - mn);
+                    M.msm[r] = mn;
+                }
+                tc::named_bar(gbar, 128);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) ls[k] *= M.alpha[rbase + k];
+                if (!first) {
+                    // O must be scaled before MMA2 of this tile adds to it
+                    tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp,
+                                  kTimeoutNs);
+                    tc::fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t to[16];
+                        tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            to[k] = __float_as_uint(__uint_as_float(to[k]) * M.alpha[rbase + 16 * cc + k]);
+                        tc::tmem_st16(lane_addr + kColO + rbase + 16u * cc, to);
+                    }
+                    tc::wait_st();
+                }
+            }
+            // -------- probabilities, running sums, P' = p * ||v|| * wscale (fp16)
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+                const float p0 = (rbase + k < R) ? ex2(x[k] - M.msm[rbase + k]) : 0.0f;
+                const float p1 = (rbase + k + 1 < R) ? ex2(x[k + 1] - M.msm[rbase + k + 1]) : 0.0f;
+                ls[k] += p0;
+                ls[k + 1] += p1;
+                const __half2 h = __floats2half2_rn(p0 * wt, p1 * wt);
+                pk[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
+            uint8_t* prow = sP + s * 16384;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4*>(prow + tc::sw128((uint32_t)tt, 16u * (4 * grp + cc))) =
+                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+            tc::fence_proxy_async();
+            tc::fence_before();
+            tc::mbar_arrive(tc::smem_u32(&M.pfull[s]));
+
+            if (last) {
+                // -------- segment epilogue: row sums, O^T, partial for (unit, piece)
+                tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph, abortp, kTimeoutNs);
+                tc::fence_after();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    float v = ls[k];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == k) M.red[grp][wq][k] = v;
+                }
+                tc::named_bar(gbar, 128);
+                const int64_t ulo = cta_of_tile(seg_u * nt, TT, P.nctas);
+                const int64_t slot = seg_u * P.pmax + (c - ulo);
+                const float unscale = 1.0f / wscale;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t to[16];
+                    tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int r = rbase + 16 * cc + k;
+                        if (r < R) P.ws_acc[(slot * R + r) * kD + tt] = __uint_as_float(to[k]) * unscale;
+                    }
+                }
+                if (tt < 32 && rbase + tt < R) {
+                    const int r = rbase + tt;
+                    P.ws_ml[(slot * R + r) * 2] = M.msm[r];
+                    P.ws_ml[(slot * R + r) * 2 + 1] =
+                        M.red[grp][0][tt] + M.red[grp][1][tt] + M.red[grp][2][tt] + M.red[grp][3][tt];
+                }
+                tc::fence_before();
+                tc::named_bar(3, 256);
+            }
+            if (*abortp) break;
+        }
+    } else if (warp == 12 && lane == 0) {
+        // =============================== MMA issuer (one thread)
+        const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);
+        const uint32_t id2 = tc::idesc_f16(128, kNR, true, true);
+        const uint32_t sq = tc::smem_u32(sQ), sv = tc::smem_u32(sV), sp = tc::smem_u32(sP);
+        auto issue_mma2 = [&](int64_t jj) -> bool {
+            const int s2 = (int)(jj & 1);
+            const uint32_t ph2 = (uint32_t)((jj >> 1) & 1);
+            const int64_t gg = g0 + jj;
+            const bool seg_first = (jj == 0) || ((gg % nt) == 0);
+            if (!tc::mbar_wait(tc::smem_u32(&M.vfull[s2]), ph2, abortp, kTimeoutNs)) return false;
+            if (!tc::mbar_wait(tc::smem_u32(&M.pfull[s2]), ph2, abortp, kTimeoutNs)) return false;
+            tc::fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t ad = tc::sdesc(sv + s2 * 32768 + ks * 2048, 16384, 1024);
+                const uint64_t bd = tc::sdesc(sp + s2 * 16384 + ks * 2048, 16384, 1024);
+                tc::mma_ss(tbase + kColO, ad, bd, id2, (seg_first && ks == 0) ? 0u : 1u);
+            }
+            tc::commit(tc::smem_u32(&M.pvfree[s2]));
+            return true;
+        };
+        int seg = -1;
+        bool ok = true;
+        for (int64_t j = 0; j < n && ok; ++j) {
+            const int64_t g = g0 + j;
+            const bool first = (j == 0) || ((g % nt) == 0);
+            const int s = (int)(j & 1);
+            const uint32_t ph = (uint32_t)((j >> 1) & 1);
+            if (first) {
+                if (j > 0 && !issue_mma2(j - 1)) break;
+                ++seg;
+                if (!tc::mbar_wait(tc::smem_u32(&M.qready), (uint32_t)(seg & 1), abortp, kTimeoutNs)) break;
+            }
+            if (!tc::mbar_wait(tc::smem_u32(&M.kfull[s]), ph, abortp, kTimeoutNs)) break;
+            if (j > 0 && !tc::mbar_wait(tc::smem_u32(&M.sfree), (uint32_t)((j - 1) & 1), abortp, kTimeoutNs)) break;
+            tc::fence_after();
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int ks = 2 * b + kk;
+                    const uint64_t bd = tc::sdesc(sq + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
+                    tc::mma_ts(tbase + kColS + 64u * b, tbase + kColK + 64u * s + 8u * ks, bd, id1, (uint32_t)kk);
+                }
+            tc::commit(tc::smem_u32(&M.sfull));
+            tc::commit(tc::smem_u32(&M.kfree[s]));
+            if (!first) ok = issue_mma2(j - 1);
+        }
+        if (ok && n > 0 && !*abortp) issue_mma2(n - 1);
+    }
+
+    // ---- tear-down: every role is past its last TMEM access
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 12) {
+        tc::fence_after();
+        tc::tmem_dealloc(tbase, kTmemCols);
+    }
+    if (tid == 0 && M.abort) atomicOr(P.p.status, 1u);
+}
+
+int g_num_sms = 0;
+
+int num_sms() {
+    if (g_num_sms == 0) {
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+        g_num_sms = v;
+    }
+    return g_num_sms;
+}
+
+struct TcPlan {
+    int64_t nt, tt;
+    int nctas, pmax;
+};
+
+TcPlan plan(const PoolView& p, int64_t n_ctx) {
+    TcPlan pl;
+    pl.nt = (n_ctx + kTile - 1) / kTile;
+    const int64_t U = (int64_t)p.L * p.H;
+    pl.tt = U * pl.nt;
+    const int64_t sms = num_sms();
+    pl.nctas = (int)(pl.tt < sms ? pl.tt : sms);
+    int pm = 1;
+    for (int64_t u = 0; u < U; ++u) {
+        const int64_t lo = ((u * pl.nt + 1) * pl.nctas - 1) / pl.tt;
+        const int64_t hi = (((u + 1) * pl.nt) * pl.nctas - 1) / pl.tt;
+        if (hi - lo + 1 > pm) pm = (int)(hi - lo + 1);
+    }
+    pl.pmax = pm;
+    return pl;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+}  // namespace
+
+bool attend_tc_supported(const PoolView& p, int rows) { return p.d == kD && rows >= 1 && rows <= kNR; }
+
+size_t attend_tc_workspace(const PoolView& p, int rows, int64_t n_ctx) {
+    const TcPlan pl = plan(p, n_ctx);
+    const size_t U = (size_t)p.L * p.H;
+    return sizeof(float) * U * (size_t)pl.pmax * (size_t)rows * (size_t)(kD + 2);
+}
+
+polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
+                               int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+    const int G = n_q_heads / p.H;
+    const int R = n_agents * G;
+    if (!attend_tc_supported(p, R)) return set_error(POLYKV_E_UNSUPPORTED, "tensor-core attend: d=%d rows=%d", p.d, R);
+    const TcPlan pl = plan(p, n_ctx);
+    const size_t need = attend_tc_workspace(p, R, n_ctx);
+    if (ws_bytes < need) return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend: workspace %zu < %zu bytes", ws_bytes, need);
+    // key codes as a 2-D [U*cap rows][128 bytes] tensor, 128-row boxes, 128B swizzle
+    const EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return set_error(POLYKV_E_CUDA, "attend_tc: cuTensorMapEncodeTiled unavailable");
+    CUtensorMap kmap;
+    const size_t U = (size_t)p.L * p.H;
+    const cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)(U * (size_t)p.cap)};
+    const cuuint64_t gstride[1] = {(cuuint64_t)kD};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kTile};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult cr = enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)p.kq, gdim, gstride, box, estride,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return set_error(POLYKV_E_CUDA, "attend_tc: tensor map encode failed (%d)", (int)cr);
+    TcParams P;
+    P.p = p;
+    P.q = static_cast<const uint16_t*>(q);
+    P.ws_acc = static_cast<float*>(ws);
+    P.ws_ml = P.ws_acc + U * (size_t)pl.pmax * (size_t)R * kD;
+    P.n_ctx = n_ctx;
+    P.total_tiles = pl.tt;
+    P.A = n_agents;
+    P.Hq = n_q_heads;
+    P.G = G;
+    P.R = R;
+    P.nt = (int)pl.nt;
+    P.nctas = pl.nctas;
+    P.pmax = pl.pmax;
+    P.scale_log2 = scale * kLog2eTc;
+    auto kern = dt == POLYKV_BF16 ? attend_tc_kernel<true> : attend_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmBytes);
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_tc: smem attribute: %s", cudaGetErrorString(e));
+    kern<<<pl.nctas, kThreadsTc, kSmBytes, stream>>>(kmap, P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_tc launch: %s", cudaGetErrorString(e));
+    return launch_attend_merge(P.ws_acc, P.ws_ml, out, (int)U, p.H, n_agents, n_q_heads, R, pl.pmax, pl.nt, pl.tt,
+                               pl.nctas, kD, stream);
+}
+
+}  // namespace polykv

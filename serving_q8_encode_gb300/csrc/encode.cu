@@ -4,136 +4,245 @@
 // for Multi-Agent LLM Inference"): keys int8 q8_0, values FWHT rotation then
 // 3-bit Lloyd-Max quantization tuned to N(0,1), written once.
 //
-// Work mapping: G = d/8 consecutive lanes own one (layer, kv head, token)
-// position; each lane loads 8 key and 8 value elements with one 16-byte load
-// each. The fp32 operation order below is fixed (the CPU oracle restates it):
-//   keys:   block amax over 4 lanes (shuffle max), s16 = fp16_rn(amax / 127),
-//           code = round-half-away(x / s16) with an IEEE division;
-//   values: ||v||^2 = lane-local left-to-right sum of rounded squares, then an
-//           xor-butterfly (pairwise tree) over the G lanes; FWHT butterflies at
-//           strides 1, 2, 4 inside the lane and 8, 16, ... across lanes, each
-//           (a, b) -> (a + b, a - b) with a the lower index; u = y / ||v||.
+// Work mapping: d/32 lanes own one (layer, kv head, token) position; each lane
+// holds one whole 32-element q8_0 block of the key and 32 consecutive value
+// coordinates (four 16-byte loads each). The fp32 operation order is fixed
+// (the CPU oracle restates it):
+//   keys:   amax over the block; s16 = fp16_rn(amax / 127) (IEEE division);
+//           code = round-half-away(x / s16), the quotient correctly rounded;
+//   values: ||v||^2 = per 8-coordinate group a left-to-right sum of rounded
+//           squares, then a pairwise tree over the d/8 group sums (two levels
+//           inside the lane, the rest by xor-shuffles); FWHT butterflies at
+//           strides 1..16 inside the lane and 32, 64 across lanes, each
+//           (a, b) -> (a + b, a - b) with a the lower index; u = y / ||v||,
+//           correctly rounded; code = number of boundaries <= u.
+// Both quotients use one IEEE reciprocal y = 1/b per divisor and two
+// residual corrections (Markstein 1990: with y correctly rounded and q
+// within one ulp, RN(q + (a - b q) y) = RN(a / b)); the first correction
+// brings q within one ulp, the second rounds correctly.
+// Pairs of fp32 lanes use Blackwell's packed f32x2 add/mul/fma, which round
+// each element exactly like the scalar instructions.
+#include <cstring>
+
 #include "polykv_internal.cuh"
 
 namespace polykv {
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4 raw, float (&x)[8], bool bf16) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+__device__ __forceinline__ uint64_t f2u(float2 a) {
+    uint64_t u;
+    memcpy(&u, &a, 8);
+    return u;
+}
+__device__ __forceinline__ float2 u2f(uint64_t u) {
+    float2 a;
+    memcpy(&a, &u, 8);
+    return a;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+    return u2f(d);
+}
+
+// correctly rounded a / b given yb = RN(1 / b) and nb = -b (pairs)
+__device__ __forceinline__ float2 div2_cr(float2 a, float2 yb, float2 nb) {
+    float2 q = mul2(a, yb);
+    float2 r = fma2(q, nb, a);
+    q = fma2(r, yb, q);
+    r = fma2(q, nb, a);
+    return fma2(r, yb, q);
+}
+
+__device__ __forceinline__ void load32(const uint16_t* src, float (&x)[32], bool bf16) {
+    const uint4* p = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
-        if (bf16) {
-            x[2 * i] = __uint_as_float(lo << 16);
-            x[2 * i + 1] = __uint_as_float(hi << 16);
-        } else {
-            x[2 * i] = __half2float(__ushort_as_half((unsigned short)lo));
-            x[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)hi));
+    for (int c = 0; c < 4; ++c) {
+        const uint4 raw = __ldcs(p + c);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (bf16) {
+                x[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+                x[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            } else {
+                const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+                const float2 f = __half22float2(h);
+                x[8 * c + 2 * i] = f.x;
+                x[8 * c + 2 * i + 1] = f.y;
+            }
         }
     }
 }
 
 __device__ __forceinline__ uint32_t value_code(float u) {
-    // number of boundaries b_i <= u, boundaries symmetric about 0
-    const uint32_t c = (u >= -kB6) + (u >= -kB5) + (u >= -kB4) + (u >= 0.0f) + (u >= kB4) + (u >= kB5) +
-                       (u >= kB6);
-    return c;
+    // number of boundaries b_i <= u (boundaries symmetric about 0)
+    return (uint32_t)(u >= -kB6) + (uint32_t)(u >= -kB5) + (uint32_t)(u >= -kB4) + (uint32_t)(u >= 0.0f) +
+           (uint32_t)(u >= kB4) + (uint32_t)(u >= kB5) + (uint32_t)(u >= kB6);
 }
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                                                      PoolView p, int64_t n_tok, int64_t t0, int64_t n_vec) {
-    constexpr int G = D / 8;             // lanes per vector
-    constexpr int VPB = 256 / G;         // vectors per block
-    const int gl = threadIdx.x % G;      // lane inside the vector group
-    const int64_t vi_raw = (int64_t)blockIdx.x * VPB + threadIdx.x / G;
+    constexpr int LPV = D / 32;          // lanes per vector
+    constexpr int VPB = 256 / LPV;       // vectors per block
+    __shared__ float s_norm[VPB];
+    const int gl = threadIdx.x % LPV;
+    const int vloc = threadIdx.x / LPV;
+    const int64_t vi_raw = (int64_t)blockIdx.x * VPB + vloc;
     const bool valid = vi_raw < n_vec;
-    const int64_t vi = valid ? vi_raw : n_vec - 1;  // keep every lane in the shuffles
+    const int64_t vi = valid ? vi_raw : n_vec - 1;   // every lane takes part in the shuffles
     const int64_t unit = vi / n_tok;
-    const int64_t tok = t0 + (vi - unit * n_tok);
-    const int64_t pidx = unit * p.cap + tok;        // pool position
+    const int64_t pidx = unit * p.cap + t0 + (vi - unit * n_tok);
 
-    const uint4 kraw = __ldcs(reinterpret_cast<const uint4*>(k + vi * D) + gl);
-    const uint4 vraw = __ldcs(reinterpret_cast<const uint4*>(v + vi * D) + gl);
-
-    // ---------------- keys: q8_0
-    float x[8];
-    unpack8(kraw, x, BF16);
-    float amax = 0.0f;
+    // ---------------- keys: one q8_0 block per lane
+    {
+        float x[32];
+        load32(k + vi * D + gl * 32, x, BF16);
+        float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
-    const float sf = __half2float(s16);
-    const bool usable = sf > 0.0f && sf <= 65504.0f;
-    uint32_t packed[2] = {0u, 0u};
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
+        const float sf = __half2float(s16);
+        const bool usable = sf > 0.0f && sf <= 65504.0f;
+        const float yb = usable ? __frcp_rn(sf) : 0.0f;
+        const float2 yb2 = make_float2(yb, yb), nb2 = make_float2(-sf, -sf);
+        uint32_t packed[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int q = 0;
-        if (usable) {
-            const float r = __fdiv_rn(x[i], sf);
-            q = (int)roundf(r);  // halfway cases away from zero
-            q = max(-127, min(127, q));
+        for (int i = 0; i < 8; ++i) packed[i] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const float2 r = div2_cr(make_float2(x[i], x[i + 1]), yb2, nb2);
+            // round half away from zero: trunc(r + copysign(0.5, r)) with the add rounded toward
+            // zero, which equals floor(|r| + 0.5) exactly for |r| < 2^22
+            const int q0 = usable ? (int)__fadd_rz(r.x, copysignf(0.5f, r.x)) : 0;
+            const int q1 = usable ? (int)__fadd_rz(r.y, copysignf(0.5f, r.y)) : 0;
+            const int c0 = max(-127, min(127, q0)), c1 = max(-127, min(127, q1));
+            packed[i >> 2] |= ((uint32_t)(c0 & 0xFF) << (8 * (i & 3))) | ((uint32_t)(c1 & 0xFF) << (8 * ((i & 3) + 1)));
         }
-        packed[i >> 2] |= (uint32_t)(q & 0xFF) << (8 * (i & 3));
+        if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.kq + pidx * D + gl * 32);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            p.ks[pidx * (D / kQ8Block) + gl] = s16;
+        }
     }
 
     // ---------------- values: norm, FWHT, 3-bit codes
-    float y[8];
-    unpack8(vraw, y, BF16);
-    float ss = __fmul_rn(y[0], y[0]);
+    float y[32];
+    load32(v + vi * D + gl * 32, y, BF16);
+    float nrm;
+    {
+        float2 sq[16];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(y[i], y[i]));
+        for (int i = 0; i < 16; ++i) sq[i] = mul2(make_float2(y[2 * i], y[2 * i + 1]), make_float2(y[2 * i], y[2 * i + 1]));
+        // groups g = 0..3 of 8 coordinates: group g's squares are sq[4g..4g+3] (.x, .y interleaved)
+        // accumulate groups (0,1) and (2,3) as packed pairs, left to right inside each group
+        float2 a01 = make_float2(sq[0].x, sq[4].x), a23 = make_float2(sq[8].x, sq[12].x);
+        a01 = add2(a01, make_float2(sq[0].y, sq[4].y));
+        a23 = add2(a23, make_float2(sq[8].y, sq[12].y));
 #pragma unroll
-    for (int m = 1; m < G; m <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
-    const float nrm = __fsqrt_rn(ss);
-
+        for (int e = 1; e < 4; ++e) {
+            a01 = add2(a01, make_float2(sq[e].x, sq[4 + e].x));
+            a23 = add2(a23, make_float2(sq[8 + e].x, sq[12 + e].x));
+            a01 = add2(a01, make_float2(sq[e].y, sq[4 + e].y));
+            a23 = add2(a23, make_float2(sq[8 + e].y, sq[12 + e].y));
+        }
+        float ss = __fadd_rn(__fadd_rn(a01.x, a01.y), __fadd_rn(a23.x, a23.y));
 #pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
+        for (int m = 1; m < LPV; m <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
+        nrm = __fsqrt_rn(ss);
+    }
+    // butterflies, stride 1 (scalar) then 2..16 (packed pairs)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 32; i += 2) {
+        const float a = y[i], b = y[i + 1];
+        y[i] = __fadd_rn(a, b);
+        y[i + 1] = __fsub_rn(a, b);
+    }
+#pragma unroll
+    for (int h = 2; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
             if ((i & h) == 0) {
-                const float a = y[i], b = y[i + h];
-                y[i] = __fadd_rn(a, b);
-                y[i + h] = __fsub_rn(a, b);
+                const float2 a = make_float2(y[i], y[i + 1]), b = make_float2(y[i + h], y[i + h + 1]);
+                const float2 s = add2(a, b), d = sub2(a, b);
+                y[i] = s.x;
+                y[i + 1] = s.y;
+                y[i + h] = d.x;
+                y[i + h + 1] = d.y;
             }
         }
     }
 #pragma unroll
-    for (int m = 1; m < G; m <<= 1) {
-        const bool upper = (gl & m) != 0;
+    for (int m = 1; m < LPV; m <<= 1) {
+        const float sg = (gl & m) ? -1.0f : 1.0f;  // upper lane: lower - upper; lower lane: lower + upper
+        const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, y[i], m);
-            y[i] = upper ? __fsub_rn(o, y[i]) : __fadd_rn(y[i], o);
+        for (int i = 0; i < 32; i += 2) {
+            const float o0 = __shfl_xor_sync(0xffffffffu, y[i], m);
+            const float o1 = __shfl_xor_sync(0xffffffffu, y[i + 1], m);
+            const float2 r = fma2(sg2, make_float2(y[i], y[i + 1]), make_float2(o0, o1));
+            y[i] = r.x;
+            y[i + 1] = r.y;
         }
     }
-    uint32_t w24 = 0;
+    const bool nz = nrm > 0.0f;
+    const float yn = nz ? __frcp_rn(nrm) : 0.0f;
+    const float2 yn2 = make_float2(yn, yn), nn2 = make_float2(-nrm, -nrm);
+    uint32_t w24[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float u = nrm > 0.0f ? __fdiv_rn(y[i], nrm) : 0.0f;
-        w24 |= value_code(u) << (3 * i);
+    for (int i = 0; i < 32; i += 2) {
+        float2 u = div2_cr(make_float2(y[i], y[i + 1]), yn2, nn2);
+        if (!nz) u = make_float2(0.0f, 0.0f);
+        w24[i >> 3] |= (value_code(u.x) << (3 * (i & 7))) | (value_code(u.y) << (3 * ((i & 7) + 1)));
     }
-    // gather 3-byte lane words into 32-bit words: word j = bytes 4j..4j+3 of the vector's codes
-    const int lo_lane = (4 * gl) / 3;
-    const int shift = 8 * (4 * gl - 3 * lo_lane);
-    const int grp_base = (threadIdx.x & 31) & ~(G - 1);
-    const uint32_t wlo = __shfl_sync(0xffffffffu, w24, grp_base + min(lo_lane, G - 1));
-    const uint32_t whi = __shfl_sync(0xffffffffu, w24, grp_base + min(lo_lane + 1, G - 1));
-    const uint32_t word = (wlo >> shift) | (whi << (24 - shift));
-
-    if (!valid) return;
-    reinterpret_cast<uint2*>(p.kq + pidx * D)[gl] = make_uint2(packed[0], packed[1]);
-    if ((gl & 3) == 0) p.ks[pidx * (D / kQ8Block) + gl / 4] = s16;
-    if (gl < 3 * G / 4) reinterpret_cast<uint32_t*>(p.vc + pidx * (3 * D / 8))[gl] = word;
-    if (gl == 0) p.vn[pidx] = __float2half_rn(nrm);
+    if (valid) {
+        // this lane's 32 codes are bits 96*gl .. 96*gl+95 of the vector's packed row
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.vc + pidx * (3 * D / 8) + gl * 12);
+        dst[0] = w24[0] | (w24[1] << 24);
+        dst[1] = (w24[1] >> 8) | (w24[2] << 16);
+        dst[2] = (w24[2] >> 16) | (w24[3] << 8);
+        if (gl == 0) p.vn[pidx] = __float2half_rn(nrm);
+    }
+    // running per-unit maximum of ||v|| (an upper bound used by attention to scale fp16 operands)
+    if (gl == 0) s_norm[vloc] = valid ? nrm : 0.0f;
+    __syncthreads();
+    if (threadIdx.x < VPB) {
+        const int64_t my = (int64_t)blockIdx.x * VPB + threadIdx.x;
+        const int64_t blk_end = (int64_t)blockIdx.x * VPB + VPB;
+        const int64_t last = (blk_end < n_vec ? blk_end : n_vec) - 1;
+        if (my <= last) {
+            const int64_t u_my = my / n_tok;
+            const bool head = threadIdx.x == 0 || ((my - 1) / n_tok) != u_my;
+            if (head) {
+                float mx = 0.0f;
+                for (int64_t w = my; w <= last && w / n_tok == u_my; ++w) mx = fmaxf(mx, s_norm[w - (int64_t)blockIdx.x * VPB]);
+                atomicMax(reinterpret_cast<unsigned int*>(p.nmax) + u_my, __float_as_uint(mx));
+            }
+        }
+    }
 }
 
 template <int D, bool BF16>
 polykv_status run(const PoolView& p, const void* k, const void* v, int64_t t0, int64_t n, cudaStream_t st) {
     const int64_t n_vec = (int64_t)p.L * p.H * n;
-    constexpr int VPB = 256 / (D / 8);
+    constexpr int VPB = 256 / (D / 32);
     const int64_t blocks = (n_vec + VPB - 1) / VPB;
     if (blocks > 0x7FFFFFFF) return set_error(POLYKV_E_UNSUPPORTED, "encode: too many vectors (%lld)", (long long)n_vec);
     encode_kernel<D, BF16><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(k),

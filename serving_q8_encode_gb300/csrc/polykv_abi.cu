@@ -4,6 +4,7 @@
 // (abstract): write one compressed pool once, let N agents attend over it.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -46,7 +47,9 @@ static polykv_status compute_regions(const polykv_pool_desc* d, polykv_pool_regi
     size_t off = 0;
     r->capacity_rounded = cap;
     r->status_off = off;
-    off = align_up(off + 256, 256);
+    r->v_nmax_off = off + 256;
+    off = align_up(off + 256 + units * sizeof(float), 256);
+    r->header_bytes = off;
     r->k_codes_off = off;
     off = align_up(off + toks * hd, 256);
     r->k_scales_off = off;
@@ -60,6 +63,21 @@ static polykv_status compute_regions(const polykv_pool_desc* d, polykv_pool_regi
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Which attention kernel serves a call: the tensor-core path for head_dim 128
+// and up to 64 rows per kv head, the CUDA-core path otherwise. The
+// environment variable POLYKV_ATTEND_PATH=simt|tc overrides (tc only where
+// supported) so both paths can be checked on the same shapes.
+static bool use_tc_path(const PoolView& p, int rows) {
+    const bool tc_ok = attend_tc_supported(p, rows);
+    const char* e = getenv("POLYKV_ATTEND_PATH");
+    if (e && strcmp(e, "simt") == 0) return false;
+    return tc_ok;
+}
+
+static size_t attend_workspace(const PoolView& p, int rows, int64_t n_ctx) {
+    return use_tc_path(p, rows) ? attend_tc_workspace(p, rows, n_ctx) : attend_simt_workspace(p, rows, n_ctx);
+}
 
 }  // namespace polykv
 
@@ -91,6 +109,7 @@ polykv_status polykv_pool_create(const polykv_pool_desc* desc, void* dev_buf, si
     p->view.vc = reinterpret_cast<uint8_t*>(base + r.v_codes_off);
     p->view.vn = reinterpret_cast<__half*>(base + r.v_norms_off);
     p->view.status = reinterpret_cast<uint32_t*>(base + r.status_off);
+    p->view.nmax = reinterpret_cast<float*>(base + r.v_nmax_off);
     p->view.L = desc->n_layers;
     p->view.H = desc->n_kv_heads;
     p->view.d = desc->head_dim;
@@ -119,6 +138,12 @@ polykv_status polykv_encode(polykv_pool* pool, const void* k, const void* v, int
     if (n_tokens == 0) return POLYKV_OK;
     if (!k || !v) return set_error(POLYKV_E_INVAL, "k and v must be non-NULL");
     if (!aligned16(k) || !aligned16(v)) return set_error(POLYKV_E_INVAL, "k and v must be 16-byte aligned");
+    if (pool->encoded == 0) {
+        // first write into this pool: clear the header (status word, per-unit norm maxima)
+        const cudaError_t e = cudaMemsetAsync(pool->view.status, 0, pool->regions.header_bytes - pool->regions.status_off,
+                                              static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "encode: header clear: %s", cudaGetErrorString(e));
+    }
     const polykv_status st =
         launch_encode(pool->view, pool->desc.in_dtype, k, v, t0, n_tokens, static_cast<cudaStream_t>(stream));
     if (st != POLYKV_OK) return st;
@@ -147,7 +172,7 @@ polykv_status polykv_attend_workspace_size(const polykv_pool* pool, int32_t n_ag
     if (st != POLYKV_OK) return st;
     if (!bytes) return set_error(POLYKV_E_INVAL, "bytes is NULL");
     const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
-    *bytes = attend_simt_workspace(pool->view, rows, n_ctx);
+    *bytes = attend_workspace(pool->view, rows, n_ctx);
     return POLYKV_OK;
 }
 
@@ -160,11 +185,28 @@ polykv_status polykv_attend(const polykv_pool* pool, const void* q, float* out, 
     if (!aligned16(q) || !aligned16(out) || (workspace && !aligned16(workspace)))
         return set_error(POLYKV_E_INVAL, "q, out and workspace must be 16-byte aligned");
     const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
-    const size_t need = attend_simt_workspace(pool->view, rows, n_ctx);
+    const size_t need = attend_workspace(pool->view, rows, n_ctx);
     if (need > 0 && !workspace) return set_error(POLYKV_E_INVAL, "workspace is NULL but %zu bytes are needed", need);
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
+    if (use_tc_path(pool->view, rows))
+        return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
+                                workspace_bytes, static_cast<cudaStream_t>(stream));
     return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
                               workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+polykv_status polykv_pool_status(const polykv_pool* pool, void* stream, uint32_t* flags) {
+    if (!pool || !flags) return set_error(POLYKV_E_INVAL, "pool and flags must be non-NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, pool->view.status, sizeof(h), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(pool->view.status, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "status read: %s", cudaGetErrorString(e));
+    *flags = h;
+    if (h & 1u) return set_error(POLYKV_E_TIMEOUT, "a kernel gave up waiting on a bounded device-side wait");
+    return POLYKV_OK;
 }
 
 polykv_status polykv_free(polykv_pool* pool) {

@@ -30,7 +30,8 @@ struct PoolView {
     __half* ks;        // [U][cap][d/32]
     uint8_t* vc;       // [U][cap][3d/8]
     __half* vn;        // [U][cap]
-    uint32_t* status;  // small status block
+    uint32_t* status;  // status word (bit 0: a bounded device wait gave up)
+    float* nmax;       // [U] running maximum of ||v|| per unit
     int L, H, d;
     int64_t cap;
 };
@@ -46,6 +47,16 @@ size_t attend_simt_workspace(const PoolView& p, int rows, int64_t n_ctx);
 polykv_status launch_attend_simt(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
                                  int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
                                  cudaStream_t stream);
+
+polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float* out, int U, int H, int A, int Hq,
+                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st);
+
+// tensor-core attention path (head_dim 128, up to 64 rows per kv head)
+bool attend_tc_supported(const PoolView& p, int rows);
+size_t attend_tc_workspace(const PoolView& p, int rows, int64_t n_ctx);
+polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
+                               int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
+                               cudaStream_t stream);
 
 __host__ __device__ inline float centroid_of(int code) {
     // ascending codes 0..7 -> -c7 .. -c4, c4 .. c7

@@ -64,7 +64,9 @@ def test_query_mode_and_layout(lib):
         assert r.v_codes_off - r.k_scales_off >= U * C * 4 * 2
         assert r.v_norms_off - r.v_codes_off >= U * C * 48
         assert r.total_bytes - r.v_norms_off >= U * C * 2
-        for off in (r.k_codes_off, r.k_scales_off, r.v_codes_off, r.v_norms_off):
+        assert r.status_off == 0 and r.v_nmax_off == 256 and r.header_bytes >= 256 + 4 * U
+        assert r.k_codes_off >= r.header_bytes
+        for off in (r.k_codes_off, r.k_scales_off, r.v_codes_off, r.v_norms_off, r.header_bytes):
             assert off % 256 == 0
     finally:
         pk.polykv_free(h)

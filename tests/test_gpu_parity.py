@@ -3,6 +3,8 @@ the same seeded inputs. Encode: q8 codes, scales, norms and 3-bit codes
 bit-exact (3-bit codes may differ only where the oracle's u lies within
 1e-6 * max(|b|, 1) of a boundary b, at most 1e-5 of elements). Attention:
 max abs error <= 2e-3 against the float64 oracle over the oracle's pool."""
+import os
+
 import numpy as np
 import pytest
 
@@ -47,6 +49,22 @@ def check_encode(pool, ref, n_tok, t_off=0, b32=None):
         assert np.array_equal(f["v_packed"][:, :, sl], ref["v_packed"])
 
 
+@pytest.fixture(params=["default", "simt"])
+def path(request):
+    """Attention kernel selection: the library's default (tensor cores for head_dim 128)
+    and the CUDA-core path forced through POLYKV_ATTEND_PATH."""
+    old = os.environ.get("POLYKV_ATTEND_PATH")
+    if request.param == "default":
+        os.environ.pop("POLYKV_ATTEND_PATH", None)
+    else:
+        os.environ["POLYKV_ATTEND_PATH"] = request.param
+    yield request.param
+    if old is None:
+        os.environ.pop("POLYKV_ATTEND_PATH", None)
+    else:
+        os.environ["POLYKV_ATTEND_PATH"] = old
+
+
 def run_case(env, L, H, Hq, d, T, A, dtype, seed=0, q_mult=1.0, n_ctx=None, layers=None, scale=0.0,
              chunks=None):
     pk, torch, c32, b32 = env
@@ -63,6 +81,7 @@ def run_case(env, L, H, Hq, d, T, A, dtype, seed=0, q_mult=1.0, n_ctx=None, laye
     n_ctx = T if n_ctx is None else n_ctx
     out = pool.attend(_dev(torch, qb), n_ctx, softmax_scale=scale)
     torch.cuda.synchronize()
+    assert pool.status() == 0
     ref_pool = oracle.attention.encode_pool(kb, vb, dtype, b32)
     check_encode(pool, ref_pool, T, 0, b32)
     ref = oracle.attention.attend_pool(qb, dtype, ref_pool, n_ctx, c32,
@@ -85,27 +104,27 @@ def test_smollm2_full_stack_1851_5_agents(env):
     run_case(env, 24, 32, 32, 64, 1851, 5, "f16", layers=[0, 5, 11, 23])
 
 
-def test_llama3_8b_4096_15_agents_sampled_layers(env):
+def test_llama3_8b_4096_15_agents_sampled_layers(env, path):
     run_case(env, 32, 8, 32, 128, 4096, 15, "bf16", layers=[0, 13, 31])
 
 
-def test_llama3_8b_7194_context(env):
+def test_llama3_8b_7194_context(env, path):
     run_case(env, 2, 8, 32, 128, 7194, 15, "bf16")
 
 
 # ---- ragged and degenerate cases
 @pytest.mark.parametrize("T", [1, 31, 33, 64, 65, 129, 257])
 @pytest.mark.parametrize("d", [64, 128])
-def test_ragged_lengths(env, T, d):
+def test_ragged_lengths(env, path, T, d):
     run_case(env, 1, 2, 8, d, T, 3, "bf16" if d == 128 else "f16", seed=T)
 
 
 @pytest.mark.parametrize("A,G", [(1, 1), (2, 4), (15, 4), (20, 4), (33, 2), (7, 1)])
-def test_rows_per_kv_head(env, A, G):
+def test_rows_per_kv_head(env, path, A, G):
     run_case(env, 2, 2, 2 * G, 128, 200, A, "bf16", seed=A)
 
 
-def test_peaky_queries_online_rescale(env):
+def test_peaky_queries_online_rescale(env, path):
     run_case(env, 2, 4, 16, 128, 1000, 4, "bf16", q_mult=8.0)
 
 
@@ -113,7 +132,7 @@ def test_very_peaky_queries(env):
     run_case(env, 1, 2, 8, 64, 700, 3, "f16", q_mult=40.0)
 
 
-def test_zero_queries_give_mean(env):
+def test_zero_queries_give_mean(env, path):
     run_case(env, 1, 2, 8, 128, 300, 2, "bf16", q_mult=0.0)
 
 
@@ -121,7 +140,7 @@ def test_custom_softmax_scale(env):
     run_case(env, 1, 4, 4, 64, 150, 2, "f16", scale=0.37)
 
 
-def test_partial_context_and_append(env):
+def test_partial_context_and_append(env, path):
     run_case(env, 2, 2, 8, 128, 500, 3, "bf16", n_ctx=333, chunks=[100, 1, 199, 200])
 
 
