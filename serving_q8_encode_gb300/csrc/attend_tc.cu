@@ -37,6 +37,7 @@
 // the CTA raises an abort flag, skips the rest of its work, waits (bounded)
 // for its copies in flight, frees its TMEM and sets the pool's status word.
 #include <cmath>
+#include <cstdlib>
 #include <cuda.h>
 
 #include "polykv_internal.cuh"
@@ -86,6 +87,7 @@ struct TcParams {
     int nt;      // tiles per unit
     int nctas;
     int pmax;    // partial slots per unit
+    int test_stall;  // test hook: the MMA thread issues nothing, so the softmax waits run out
     float scale_log2;
 };
 
@@ -99,7 +101,7 @@ struct Misc {
     int flags[2][3];
     int abort;
     int pad;
-    uint64_t kfull[2], kfree[2], vfull[2], pfull[2], pvfree[2], sfull, sfree, qready;
+    uint64_t kfull[2], kfree[2], vfull[2], pfull[2], pvfree[2], sfull, sfree, qready, done;
     uint64_t rfull[kNS], rempty[kNS];
     uint32_t tslot;
 };
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc::mbar_init(tc::smem_u32(&M.sfull), 1);
         tc::mbar_init(tc::smem_u32(&M.sfree), 256);
         tc::mbar_init(tc::smem_u32(&M.qready), 1);
+        tc::mbar_init(tc::smem_u32(&M.done), 1);
         M.abort = 0;
         for (int g = 0; g < 2; ++g) M.flags[g][0] = M.flags[g][1] = M.flags[g][2] = 0;
         tc::mbar_init_fence();
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // =============================== TMA: pool tiles into the ring
         if (lane == 0) {
             int64_t issued = 0;
-            for (int64_t j = 0; j < n; ++j) {
+            for (int64_t j = 0; j < n && !*abortp; ++j) {
                 const int st = (int)(j % kNS);
                 if (j >= kNS &&
                     !tc::mbar_wait(tc::smem_u32(&M.rempty[st]), (uint32_t)(((j / kNS) - 1) & 1), abortp, kTimeoutNs))
@@ -395,8 +398,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const float wscale = M.wscale;
             const int64_t tok = ti * kTile + tt;
             const bool valid = tok < P.n_ctx;
-            // per-token block scales and norm from the ring
-            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
+            // per-token block scales and norm from the ring (after an abort the waits return at once and the
+            // loop runs to the end with garbage, so both row groups pass the same named barriers)
+            tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs);
             const uint8_t* raw = sR + st * kRawStage;
             const uint2 sr = *reinterpret_cast<const uint2*>(raw + kRawS + tt * 8);
             const unsigned short nb = *reinterpret_cast<const unsigned short*>(raw + kRawN + tt * 2);
@@ -535,7 +539,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 tc::fence_before();
                 tc::named_bar(3, 256);
             }
-            if (*abortp) break;
         }
     } else if (warp == 12 && lane == 0) {
         // =============================== MMA issuer (one thread)
@@ -560,7 +563,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             return true;
         };
         int seg = -1;
-        bool ok = true;
+        bool ok = P.test_stall == 0;
         for (int64_t j = 0; j < n && ok; ++j) {
             const int64_t g = g0 + j;
             const bool first = (j == 0) || ((g % nt) == 0);
@@ -587,6 +590,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (!first) ok = issue_mma2(j - 1);
         }
         if (ok && n > 0 && !*abortp) issue_mma2(n - 1);
+        if (P.test_stall) *abortp = 0;  // let the other roles discover the stall on their own waits
+        if (n > 0) {
+            // every MMA this thread issued must have completed before the TMEM is freed
+            tc::commit(tc::smem_u32(&M.done));
+            volatile int dummy = 0;
+            tc::mbar_wait(tc::smem_u32(&M.done), 0u, &dummy, 50000000ull);
+        }
     }
 
     // ---- tear-down: every role is past its last TMEM access
@@ -697,6 +707,10 @@ polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q
     P.nctas = pl.nctas;
     P.pmax = pl.pmax;
     P.scale_log2 = scale * kLog2eTc;
+    // Test hook for the bounded-wait path: POLYKV_TEST_STALL=1 makes every wait on the tensor-core
+    // results run out; the CTA then gives up, releases its TMEM and sets the pool's status word.
+    const char* stall = getenv("POLYKV_TEST_STALL");
+    P.test_stall = (stall && stall[0] == '1') ? 1 : 0;
     auto kern = dt == POLYKV_BF16 ? attend_tc_kernel<true> : attend_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmBytes);
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_tc: smem attribute: %s", cudaGetErrorString(e));
