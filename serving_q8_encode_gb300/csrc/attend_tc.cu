@@ -38,6 +38,7 @@
 // for its copies in flight, frees its TMEM and sets the pool's status word.
 #include <cmath>
 #include <cstdlib>
+#include <cstring>
 #include <cuda.h>
 
 #include "polykv_internal.cuh"
@@ -115,6 +116,37 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ uint64_t f2u(float2 a) {
+    uint64_t u;
+    memcpy(&u, &a, 8);
+    return u;
+}
+__device__ __forceinline__ float2 u2f(uint64_t u) {
+    float2 a;
+    memcpy(&a, &u, 8);
+    return a;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+    return u2f(d);
+}
+
 // int8 x4 -> two fp16x2 words, exactly: fp16(0x6400 | (x ^ 0x80)) = 1024 + x + 128.
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
     const uint32_t u = w ^ 0x80808080u;
@@ -158,7 +190,7 @@ __device__ __forceinline__ void store_v_chunks(const uint32_t (&w)[12], const ui
 }
 
 template <bool QBF16>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+__global__ void __maxnreg__(144)
     attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u = tc::smem_u32(smem_raw);
@@ -301,7 +333,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int rbase = 32 * grp;
         int seg = -1;
         int64_t seg_u = -1;
-        float ls[32];
+        float2 ls2[16];
         for (int64_t j = 0; j < n; ++j) {
             const int64_t g = g0 + j;
             const int64_t u = g / nt;
@@ -387,12 +419,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     M.scale_eff = P.scale_log2 / fq;
                     M.wscale = nmax > 0.0f ? ldexpf(1.0f, 8 - en) : 1.0f;  // ||v|| * wscale < 2^8
                 }
-                if (si < kNR) M.msm[si] = -INFINITY;
+                if (si < kNR) M.msm[si] = si < R ? -INFINITY : INFINITY;
                 tc::fence_proxy_async();
                 tc::named_bar(3, 256);
                 if (si == 0) tc::mbar_arrive(tc::smem_u32(&M.qready));
 #pragma unroll
-                for (int k = 0; k < 32; ++k) ls[k] = 0.0f;
+                for (int k = 0; k < 16; ++k) ls2[k] = make_float2(0.0f, 0.0f);
             }
             const float scale_eff = M.scale_eff;
             const float wscale = M.wscale;
@@ -410,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const float sb[4] = {s01.x * scale_eff, s01.y * scale_eff, s23.x * scale_eff, s23.y * scale_eff};
             const float wt = valid ? __half2float(__ushort_as_half(nb)) * wscale : 0.0f;
             // -------- logits from the four block accumulators (this group's 32 rows)
-            float x[32];
+            float2 x2[16];
             tc::mbar_wait(tc::smem_u32(&M.sfull), (uint32_t)(j & 1), abortp, kTimeoutNs);
             tc::fence_after();
 #pragma unroll
@@ -419,38 +451,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 0u, t0);
                 tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 16u, t1);
                 tc::wait_ld();
+                const float2 sb2 = make_float2(sb[b], sb[b]);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    if (b == 0) {
-                        x[k] = sb[0] * __uint_as_float(t0[k]);
-                        x[16 + k] = sb[0] * __uint_as_float(t1[k]);
-                    } else {
-                        x[k] = fmaf(sb[b], __uint_as_float(t0[k]), x[k]);
-                        x[16 + k] = fmaf(sb[b], __uint_as_float(t1[k]), x[16 + k]);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    const float2 a0 = make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1]));
+                    const float2 a1 = make_float2(__uint_as_float(t1[2 * k]), __uint_as_float(t1[2 * k + 1]));
+                    x2[k] = b == 0 ? mul2(sb2, a0) : fma2(sb2, a0, x2[k]);
+                    x2[8 + k] = b == 0 ? mul2(sb2, a1) : fma2(sb2, a1, x2[8 + k]);
                 }
             }
             tc::fence_before();
             tc::mbar_arrive(tc::smem_u32(&M.sfree));
             if (!valid) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) x[k] = -INFINITY;
+                for (int k = 0; k < 16; ++k) x2[k] = make_float2(-INFINITY, -INFINITY);
             }
-            // -------- lazy rescale decision (per row group)
-            bool need = false;
+            // -------- lazy rescale decision (per row group); rows >= R carry m = +inf
+            const float2* msm2 = reinterpret_cast<const float2*>(&M.msm[rbase]);
+            float dmax = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-                if (rbase + k < R) need |= (x[k] - M.msm[rbase + k] > kTau);
+            for (int k = 0; k < 16; ++k) {
+                const float2 d = sub2(x2[k], msm2[k]);
+                dmax = fmaxf(dmax, fmaxf(d.x, d.y));
+            }
             if (tt == 0) M.flags[grp][(j + 1) % 3] = 0;
-            if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&M.flags[grp][j % 3], 1);
+            if (__any_sync(0xffffffffu, dmax > kTau) && lane == 0) atomicOr(&M.flags[grp][j % 3], 1);
             tc::named_bar(gbar, 128);
             if (M.flags[grp][j % 3]) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    float v = x[k];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                    if (lane == k) M.red[grp][wq][k] = v;
+                for (int k = 0; k < 16; ++k) {
+                    const float v0 = tc::warp_max(x2[k].x);
+                    const float v1 = tc::warp_max(x2[k].y);
+                    if (lane == 2 * k) M.red[grp][wq][2 * k] = v0;
+                    if (lane == 2 * k + 1) M.red[grp][wq][2 * k + 1] = v1;
                 }
                 tc::named_bar(gbar, 128);
                 if (tt < 32) {
@@ -459,12 +492,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
                                            fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
                     const float mn = fmaxf(mo, mt);
-                    M.alpha[r] = (mo == -INFINITY || mn == -INFINITY) ? 0.0f : ex2(mo - mn);
+                    M.alpha[r] = mo == -INFINITY ? 0.0f : (mo == mn ? 1.0f : ex2(mo - mn));
                     M.msm[r] = mn;
                 }
                 tc::named_bar(gbar, 128);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) ls[k] *= M.alpha[rbase + k];
+                for (int k = 0; k < 16; ++k) {
+                    const float2 a = make_float2(M.alpha[rbase + 2 * k], M.alpha[rbase + 2 * k + 1]);
+                    ls2[k] = mul2(ls2[k], a);
+                }
                 if (!first) {
                     // O must be scaled before MMA2 of this tile adds to it
                     tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp,
@@ -485,14 +521,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             // -------- probabilities, running sums, P' = p * ||v|| * wscale (fp16)
             uint32_t pk[16];
+            const float2 wt2 = make_float2(wt, wt);
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-                const float p0 = (rbase + k < R) ? ex2(x[k] - M.msm[rbase + k]) : 0.0f;
-                const float p1 = (rbase + k + 1 < R) ? ex2(x[k + 1] - M.msm[rbase + k + 1]) : 0.0f;
-                ls[k] += p0;
-                ls[k + 1] += p1;
-                const __half2 h = __floats2half2_rn(p0 * wt, p1 * wt);
-                pk[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int k = 0; k < 16; ++k) {
+                const float2 d = sub2(x2[k], msm2[k]);
+                const float2 p = make_float2(ex2(d.x), ex2(d.y));
+                ls2[k] = add2(ls2[k], p);
+                const float2 pw = mul2(p, wt2);
+                const __half2 h = __floats2half2_rn(pw.x, pw.y);
+                pk[k] = *reinterpret_cast<const uint32_t*>(&h);
             }
             if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
             uint8_t* prow = sP + s * 16384;
@@ -510,7 +547,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 tc::fence_after();
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    float v = ls[k];
+                    float v = (k & 1) ? ls2[k >> 1].y : ls2[k >> 1].x;
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
                     if (lane == k) M.red[grp][wq][k] = v;

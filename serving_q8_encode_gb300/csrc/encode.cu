@@ -69,12 +69,16 @@ __device__ __forceinline__ float2 div2_cr(float2 a, float2 yb, float2 nb) {
     return fma2(r, yb, q);
 }
 
-__device__ __forceinline__ void load32(const uint16_t* src, float (&x)[32], bool bf16) {
+__device__ __forceinline__ void fetch32(const uint16_t* src, uint4 (&raw)[4]) {
     const uint4* p = reinterpret_cast<const uint4*>(src);
 #pragma unroll
+    for (int c = 0; c < 4; ++c) raw[c] = __ldcs(p + c);
+}
+
+__device__ __forceinline__ void unpack32(const uint4 (&raw)[4], float (&x)[32], bool bf16) {
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint4 raw = __ldcs(p + c);
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (bf16) {
@@ -110,10 +114,15 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
     const int64_t unit = vi / n_tok;
     const int64_t pidx = unit * p.cap + t0 + (vi - unit * n_tok);
 
+    // both 64-byte rows are requested before any arithmetic (one memory round trip per lane)
+    uint4 kraw[4], vraw[4];
+    fetch32(k + vi * D + gl * 32, kraw);
+    fetch32(v + vi * D + gl * 32, vraw);
+
     // ---------------- keys: one q8_0 block per lane
     {
         float x[32];
-        load32(k + vi * D + gl * 32, x, BF16);
+        unpack32(kraw, x, BF16);
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
@@ -145,7 +154,7 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
 
     // ---------------- values: norm, FWHT, 3-bit codes
     float y[32];
-    load32(v + vi * D + gl * 32, y, BF16);
+    unpack32(vraw, y, BF16);
     float nrm;
     {
         float2 sq[16];

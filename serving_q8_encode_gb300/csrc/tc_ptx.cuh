@@ -102,21 +102,36 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` while the phase is pending
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with `parity` to complete, giving up after ~timeout_ns.
 // On give-up (or if another role already gave up) it sets *abort and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > timeout_ns) {
-                *abort = 1;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_suspend(bar, parity, 2000u)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > timeout_ns) {
+            *abort = 1;
+            return false;
         }
     }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
