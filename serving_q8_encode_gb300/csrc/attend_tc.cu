@@ -75,6 +75,7 @@ static_assert(kSmBytes <= 232448, "shared memory budget");
 constexpr uint32_t kColK = 0;     // 2 stages x 64
 constexpr uint32_t kColS = 128;   // 4 blocks x 64
 constexpr uint32_t kColO = 384;   // 64
+constexpr uint32_t kColL = 448;   // 64: per-token-slot partial row sums (lane = token slot)
 constexpr uint32_t kTmemCols = 512;
 
 struct TcParams {
@@ -189,8 +190,48 @@ __device__ __forceinline__ void store_v_chunks(const uint32_t (&w)[12], const ui
     }
 }
 
+// Lazy-rescale path of the softmax (rare): with the tile's per-warp row maxima in
+// M.red, the new running max per row of this group, alpha = 2^(m_old - m_new), and
+// O and the per-slot row sums scaled by alpha once MMA2 of the previous tile is done.
+__device__ __noinline__ void softmax_rescale(Misc& M, int grp, int wq, int tt, int rbase, uint32_t gbar, bool first,
+                                             int64_t j, uint32_t lane_addr, volatile int* abortp) {
+                tc::named_bar(gbar, 128);
+                if (tt < 32) {
+                    const int r = rbase + tt;
+                    const float mo = M.msm[r];
+                    const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
+                                           fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
+                    const float mn = fmaxf(mo, mt);
+                    M.alpha[r] = mo == -INFINITY ? 0.0f : (mo == mn ? 1.0f : ex2(mo - mn));
+                    M.msm[r] = mn;
+                }
+                tc::named_bar(gbar, 128);
+                if (!first) {
+                    // O must be scaled before MMA2 of this tile adds to it
+                    tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp,
+                                  kTimeoutNs);
+                    tc::fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t to[16], tl[16];
+                        tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
+                        tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float a = M.alpha[rbase + 16 * cc + k];
+                            to[k] = __float_as_uint(__uint_as_float(to[k]) * a);
+                            tl[k] = __float_as_uint(__uint_as_float(tl[k]) * a);
+                        }
+                        tc::tmem_st16(lane_addr + kColO + rbase + 16u * cc, to);
+                        tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
+                    }
+                    tc::wait_st();
+                }
+            }
+
 template <bool QBF16>
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(kThreadsTc, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u = tc::smem_u32(smem_raw);
@@ -333,7 +374,6 @@ __global__ void __maxnreg__(144)
         const int rbase = 32 * grp;
         int seg = -1;
         int64_t seg_u = -1;
-        float2 ls2[16];
         for (int64_t j = 0; j < n; ++j) {
             const int64_t g = g0 + j;
             const int64_t u = g / nt;
@@ -423,8 +463,6 @@ __global__ void __maxnreg__(144)
                 tc::fence_proxy_async();
                 tc::named_bar(3, 256);
                 if (si == 0) tc::mbar_arrive(tc::smem_u32(&M.qready));
-#pragma unroll
-                for (int k = 0; k < 16; ++k) ls2[k] = make_float2(0.0f, 0.0f);
             }
             const float scale_eff = M.scale_eff;
             const float wscale = M.wscale;
@@ -447,17 +485,17 @@ __global__ void __maxnreg__(144)
             tc::fence_after();
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                uint32_t t0[16], t1[16];
-                tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 0u, t0);
-                tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 16u, t1);
-                tc::wait_ld();
                 const float2 sb2 = make_float2(sb[b], sb[b]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 a0 = make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1]));
-                    const float2 a1 = make_float2(__uint_as_float(t1[2 * k]), __uint_as_float(t1[2 * k + 1]));
-                    x2[k] = b == 0 ? mul2(sb2, a0) : fma2(sb2, a0, x2[k]);
-                    x2[8 + k] = b == 0 ? mul2(sb2, a1) : fma2(sb2, a1, x2[8 + k]);
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t t0[16];
+                    tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 16u * cc, t0);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float2 a0 = make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1]));
+                        x2[8 * cc + k] = b == 0 ? mul2(sb2, a0) : fma2(sb2, a0, x2[8 * cc + k]);
+                    }
                 }
             }
             tc::fence_before();
@@ -478,6 +516,7 @@ __global__ void __maxnreg__(144)
             if (__any_sync(0xffffffffu, dmax > kTau) && lane == 0) atomicOr(&M.flags[grp][j % 3], 1);
             tc::named_bar(gbar, 128);
             if (M.flags[grp][j % 3]) {
+                // tile maximum of every row of this group (warp reduction per row, then across warps)
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const float v0 = tc::warp_max(x2[k].x);
@@ -485,51 +524,34 @@ __global__ void __maxnreg__(144)
                     if (lane == 2 * k) M.red[grp][wq][2 * k] = v0;
                     if (lane == 2 * k + 1) M.red[grp][wq][2 * k + 1] = v1;
                 }
-                tc::named_bar(gbar, 128);
-                if (tt < 32) {
-                    const int r = rbase + tt;
-                    const float mo = M.msm[r];
-                    const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
-                                           fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
-                    const float mn = fmaxf(mo, mt);
-                    M.alpha[r] = mo == -INFINITY ? 0.0f : (mo == mn ? 1.0f : ex2(mo - mn));
-                    M.msm[r] = mn;
-                }
-                tc::named_bar(gbar, 128);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float2 a = make_float2(M.alpha[rbase + 2 * k], M.alpha[rbase + 2 * k + 1]);
-                    ls2[k] = mul2(ls2[k], a);
-                }
-                if (!first) {
-                    // O must be scaled before MMA2 of this tile adds to it
-                    tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp,
-                                  kTimeoutNs);
-                    tc::fence_after();
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t to[16];
-                        tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            to[k] = __float_as_uint(__uint_as_float(to[k]) * M.alpha[rbase + 16 * cc + k]);
-                        tc::tmem_st16(lane_addr + kColO + rbase + 16u * cc, to);
-                    }
-                    tc::wait_st();
-                }
+                softmax_rescale(M, grp, wq, tt, rbase, gbar, first, j, lane_addr, abortp);
             }
             // -------- probabilities, running sums, P' = p * ||v|| * wscale (fp16)
             uint32_t pk[16];
             const float2 wt2 = make_float2(wt, wt);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float2 d = sub2(x2[k], msm2[k]);
-                const float2 p = make_float2(ex2(d.x), ex2(d.y));
-                ls2[k] = add2(ls2[k], p);
-                const float2 pw = mul2(p, wt2);
-                const __half2 h = __floats2half2_rn(pw.x, pw.y);
-                pk[k] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t tl[16];
+                if (!first) tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
+#pragma unroll
+                for (int k = 8 * cc; k < 8 * cc + 8; ++k) {
+                    const float2 d = sub2(x2[k], msm2[k]);
+                    x2[k] = make_float2(ex2(d.x), ex2(d.y));    // x2 now holds p
+                    const float2 pw = mul2(x2[k], wt2);
+                    const __half2 h = __floats2half2_rn(pw.x, pw.y);
+                    pk[k] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                if (!first) tc::wait_ld();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float2 p = x2[8 * cc + k];
+                    float2 l = first ? make_float2(0.0f, 0.0f)
+                                     : make_float2(__uint_as_float(tl[2 * k]), __uint_as_float(tl[2 * k + 1]));
+                    l = add2(l, p);
+                    tl[2 * k] = __float_as_uint(l.x);
+                    tl[2 * k + 1] = __float_as_uint(l.y);
+                }
+                tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
             }
             if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
             uint8_t* prow = sP + s * 16384;
@@ -545,12 +567,19 @@ __global__ void __maxnreg__(144)
                 // -------- segment epilogue: row sums, O^T, partial for (unit, piece)
                 tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph, abortp, kTimeoutNs);
                 tc::fence_after();
+                tc::wait_st();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    float v = (k & 1) ? ls2[k >> 1].y : ls2[k >> 1].x;
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t tl[16];
+                    tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
+                    tc::wait_ld();
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == k) M.red[grp][wq][k] = v;
+                    for (int k = 0; k < 16; ++k) {
+                        float v = __uint_as_float(tl[k]);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                        if (lane == 16 * cc + k) M.red[grp][wq][16 * cc + k] = v;
+                    }
                 }
                 tc::named_bar(gbar, 128);
                 const int64_t ulo = cta_of_tile(seg_u * nt, TT, P.nctas);
