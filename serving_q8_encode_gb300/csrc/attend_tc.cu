@@ -289,15 +289,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (warp == 13) {
         // =============================== TMA: pool tiles into the ring
         if (lane == 0) {
-            int64_t issued = 0;
-            for (int64_t j = 0; j < n && !*abortp; ++j) {
-                const int st = (int)(j % kNS);
+            int issued = 0;
+            int64_t u = g0 / nt;
+            int ti = (int)(g0 - u * nt);
+            for (int j = 0; j < (int)n && !*abortp; ++j) {
+                const int st = j & (kNS - 1);
                 if (j >= kNS &&
                     !tc::mbar_wait(tc::smem_u32(&M.rempty[st]), (uint32_t)(((j / kNS) - 1) & 1), abortp, kTimeoutNs))
                     break;
-                const int64_t g = g0 + j;
-                const int64_t u = g / nt;
-                const int64_t row0 = u * cap + (g - u * nt) * kTile;
+                const int64_t row0 = u * cap + (int64_t)ti * kTile;
+                if (++ti == nt) {
+                    ti = 0;
+                    ++u;
+                }
                 const uint32_t dst = tc::smem_u32(sR + st * kRawStage);
                 const uint32_t bar = tc::smem_u32(&M.rfull[st]);
                 tc::mbar_arrive_expect_tx(bar, kRawBytes);
@@ -308,23 +312,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 issued = j + 1;
             }
             // drain: never leave copies in flight into shared memory that is about to be released
-            for (int64_t j = issued > kNS ? issued - kNS : 0; j < issued; ++j) {
+            for (int j = issued > kNS ? issued - kNS : 0; j < issued; ++j) {
                 volatile int dummy = 0;
-                tc::mbar_wait(tc::smem_u32(&M.rfull[j % kNS]), (uint32_t)((j / kNS) & 1), &dummy, 50000000ull);
+                tc::mbar_wait(tc::smem_u32(&M.rfull[j & (kNS - 1)]), (uint32_t)((j / kNS) & 1), &dummy, 50000000ull);
             }
         }
     } else if (warp < 4) {
         // =============================== producers
         const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
         const uint32_t t = (uint32_t)tid;
-        for (int64_t j = 0; j < n && !*abortp; ++j) {
-            const int64_t g = g0 + j;
-            const int64_t u = g / nt;
-            const int64_t ti = g - u * nt;
-            const int s = (int)(j & 1);
+        int ti_next = (int)(g0 % nt);
+        for (int j = 0; j < (int)n && !*abortp; ++j) {
+            const int ti = ti_next;
+            if (++ti_next == nt) ti_next = 0;
+            const int s = j & 1;
             const uint32_t ph = (uint32_t)((j >> 1) & 1);
-            const int st = (int)(j % kNS);
-            const bool valid = ti * kTile + t < P.n_ctx;
+            const int st = j & (kNS - 1);
+            const bool valid = (int64_t)ti * kTile + t < P.n_ctx;
             if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
             const uint8_t* raw = sR + st * kRawStage;
             // keys: int8 codes -> fp16 -> TMEM lane = token
@@ -374,15 +378,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int rbase = 32 * grp;
         int seg = -1;
         int64_t seg_u = -1;
-        for (int64_t j = 0; j < n; ++j) {
-            const int64_t g = g0 + j;
-            const int64_t u = g / nt;
-            const int64_t ti = g - u * nt;
-            const int s = (int)(j & 1);
+        int64_t u = g0 / nt;
+        int ti = (int)(g0 - u * nt) - 1;
+        int f3 = 0;  // j mod 3
+        for (int j = 0; j < (int)n; ++j, f3 = (f3 == 2 ? 0 : f3 + 1)) {
+            if (++ti == nt) {
+                ti = 0;
+                ++u;
+            }
+            const int s = j & 1;
             const uint32_t ph = (uint32_t)((j >> 1) & 1);
-            const int st = (int)(j % kNS);
+            const int st = j & (kNS - 1);
             const bool first = (j == 0) || (ti == 0);
-            const bool last = (j == n - 1) || (ti == nt - 1);
+            const bool last = (j == (int)n - 1) || (ti == nt - 1);
             if (first) {
                 // -------- segment prologue (both groups): queries, operand scales, row state
                 ++seg;
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             const float scale_eff = M.scale_eff;
             const float wscale = M.wscale;
-            const int64_t tok = ti * kTile + tt;
+            const int64_t tok = (int64_t)ti * kTile + tt;
             const bool valid = tok < P.n_ctx;
             // per-token block scales and norm from the ring (after an abort the waits return at once and the
             // loop runs to the end with garbage, so both row groups pass the same named barriers)
@@ -512,10 +520,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 const float2 d = sub2(x2[k], msm2[k]);
                 dmax = fmaxf(dmax, fmaxf(d.x, d.y));
             }
-            if (tt == 0) M.flags[grp][(j + 1) % 3] = 0;
-            if (__any_sync(0xffffffffu, dmax > kTau) && lane == 0) atomicOr(&M.flags[grp][j % 3], 1);
+            if (tt == 0) M.flags[grp][f3 == 2 ? 0 : f3 + 1] = 0;
+            if (__any_sync(0xffffffffu, dmax > kTau) && lane == 0) atomicOr(&M.flags[grp][f3], 1);
             tc::named_bar(gbar, 128);
-            if (M.flags[grp][j % 3]) {
+            if (M.flags[grp][f3]) {
                 // tile maximum of every row of this group (warp reduction per row, then across warps)
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
@@ -611,11 +619,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);
         const uint32_t id2 = tc::idesc_f16(128, kNR, true, true);
         const uint32_t sq = tc::smem_u32(sQ), sv = tc::smem_u32(sV), sp = tc::smem_u32(sP);
-        auto issue_mma2 = [&](int64_t jj) -> bool {
-            const int s2 = (int)(jj & 1);
+        auto issue_mma2 = [&](int jj, bool seg_first) -> bool {
+            const int s2 = jj & 1;
             const uint32_t ph2 = (uint32_t)((jj >> 1) & 1);
-            const int64_t gg = g0 + jj;
-            const bool seg_first = (jj == 0) || ((gg % nt) == 0);
             if (!tc::mbar_wait(tc::smem_u32(&M.vfull[s2]), ph2, abortp, kTimeoutNs)) return false;
             if (!tc::mbar_wait(tc::smem_u32(&M.pfull[s2]), ph2, abortp, kTimeoutNs)) return false;
             tc::fence_after();
@@ -630,13 +636,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         };
         int seg = -1;
         bool ok = P.test_stall == 0;
-        for (int64_t j = 0; j < n && ok; ++j) {
-            const int64_t g = g0 + j;
-            const bool first = (j == 0) || ((g % nt) == 0);
-            const int s = (int)(j & 1);
+        int ti = (int)(g0 % nt) - 1;
+        bool prev_first = false;
+        for (int j = 0; j < (int)n && ok; ++j) {
+            if (++ti == nt) ti = 0;
+            const bool first = (j == 0) || (ti == 0);
+            const int s = j & 1;
             const uint32_t ph = (uint32_t)((j >> 1) & 1);
             if (first) {
-                if (j > 0 && !issue_mma2(j - 1)) break;
+                if (j > 0 && !issue_mma2(j - 1, prev_first)) break;
                 ++seg;
                 if (!tc::mbar_wait(tc::smem_u32(&M.qready), (uint32_t)(seg & 1), abortp, kTimeoutNs)) break;
             }
@@ -653,9 +661,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
             tc::commit(tc::smem_u32(&M.sfull));
             tc::commit(tc::smem_u32(&M.kfree[s]));
-            if (!first) ok = issue_mma2(j - 1);
+            if (!first) ok = issue_mma2(j - 1, prev_first);
+            prev_first = first;
         }
-        if (ok && n > 0 && !*abortp) issue_mma2(n - 1);
+        if (ok && n > 0 && !*abortp) issue_mma2((int)n - 1, prev_first);
         if (P.test_stall) *abortp = 0;  // let the other roles discover the stall on their own waits
         if (n > 0) {
             // every MMA this thread issued must have completed before the TMEM is freed

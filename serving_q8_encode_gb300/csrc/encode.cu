@@ -94,10 +94,26 @@ __device__ __forceinline__ void unpack32(const uint4 (&raw)[4], float (&x)[32], 
     }
 }
 
+__device__ __forceinline__ uint32_t ge_mask(float a, float b) {
+    uint32_t m;  // 0xFFFFFFFF if a >= b else 0
+    asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
+    return m;
+}
+
 __device__ __forceinline__ uint32_t value_code(float u) {
-    // number of boundaries b_i <= u (boundaries symmetric about 0)
-    return (uint32_t)(u >= -kB6) + (uint32_t)(u >= -kB5) + (uint32_t)(u >= -kB4) + (uint32_t)(u >= 0.0f) +
-           (uint32_t)(u >= kB4) + (uint32_t)(u >= kB5) + (uint32_t)(u >= kB6);
+    // number of boundaries b_i <= u (boundaries symmetric about 0): minus the sum of seven masks
+    const uint32_t s = ge_mask(u, -kB6) + ge_mask(u, -kB5) + ge_mask(u, -kB4) + ge_mask(u, 0.0f) + ge_mask(u, kB4) +
+                       ge_mask(u, kB5) + ge_mask(u, kB6);
+    return 0u - s;
+}
+
+__device__ __forceinline__ uint32_t bytes4(int a, int b, int c, int d) {
+    // low bytes of four ints -> one word (a in byte 0)
+    uint32_t ab, cd, w;
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(ab) : "r"(a), "r"(b));
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(cd) : "r"(c), "r"(d));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(ab), "r"(cd));
+    return w;
 }
 
 template <int D, bool BF16>
@@ -128,21 +144,21 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
         const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
         const float sf = __half2float(s16);
+        // a block whose scale is 0 or not finite gets zero codes: with yb = nb = 0 the quotient below is 0
         const bool usable = sf > 0.0f && sf <= 65504.0f;
         const float yb = usable ? __frcp_rn(sf) : 0.0f;
-        const float2 yb2 = make_float2(yb, yb), nb2 = make_float2(-sf, -sf);
+        const float2 yb2 = make_float2(yb, yb), nb2 = make_float2(usable ? -sf : 0.0f, usable ? -sf : 0.0f);
         uint32_t packed[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) packed[i] = 0u;
+        int cq[4];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
             const float2 r = div2_cr(make_float2(x[i], x[i + 1]), yb2, nb2);
             // round half away from zero: trunc(r + copysign(0.5, r)) with the add rounded toward
-            // zero, which equals floor(|r| + 0.5) exactly for |r| < 2^22
-            const int q0 = usable ? (int)__fadd_rz(r.x, copysignf(0.5f, r.x)) : 0;
-            const int q1 = usable ? (int)__fadd_rz(r.y, copysignf(0.5f, r.y)) : 0;
-            const int c0 = max(-127, min(127, q0)), c1 = max(-127, min(127, q1));
-            packed[i >> 2] |= ((uint32_t)(c0 & 0xFF) << (8 * (i & 3))) | ((uint32_t)(c1 & 0xFF) << (8 * ((i & 3) + 1)));
+            // zero, which equals floor(|r| + 0.5) exactly for |r| < 2^22; then clamp to [-127, 127]
+            // (binds only when s16 is an fp16 subnormal rounded well below amax / 127)
+            cq[i & 3] = max(-127, min(127, (int)__fadd_rz(r.x, copysignf(0.5f, r.x))));
+            cq[(i & 3) + 1] = max(-127, min(127, (int)__fadd_rz(r.y, copysignf(0.5f, r.y))));
+            if ((i & 3) == 2) packed[i >> 2] = bytes4(cq[0], cq[1], cq[2], cq[3]);
         }
         if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.kq + pidx * D + gl * 32);

@@ -193,3 +193,22 @@ def test_two_pools_interleaved_streams(env):
         o2 = pool.attend(q, T, workspace=ws2, stream=s2)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+def test_tiny_key_blocks_subnormal_scales(env):
+    """Blocks whose scale amax/127 falls into (or below) the fp16 subnormal range:
+    zero scales, and scales rounded far below amax/127 where the [-127, 127] clamp binds."""
+    pk, torch, c32, b32 = env
+    L, H, d, T = 1, 2, 128, 96
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((L, H, T, d)).astype(np.float32)
+    mags = np.array([1e-9, 3e-8, 2e-7, 1e-6, 1e-5, 1.0], np.float32)
+    k *= mags[rng.integers(0, len(mags), (L, H, T, d // 32))].repeat(32, axis=-1)
+    kb = synth.f32_to_bf16_bits(k)
+    vb = synth.f32_to_bf16_bits(rng.standard_normal((L, H, T, d)).astype(np.float32))
+    pool = pk.Pool(L, H, d, T, "bf16")
+    pool.encode(_dev(torch, kb), _dev(torch, vb))
+    torch.cuda.synchronize()
+    ref = oracle.attention.encode_pool(kb, vb, "bf16", b32)
+    assert np.any(np.abs(ref["k_codes"].astype(int)) == 127)
+    check_encode(pool, ref, T, 0, b32)

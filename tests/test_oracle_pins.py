@@ -400,3 +400,16 @@ def test_planted_half_even_rounding_is_caught():
     want = np.array([int(r[2]) for r in rows])
     half_even = np.round(x / 0.0625).astype(int)
     assert not np.array_equal(half_even, want)
+
+
+def test_q8_subnormal_scale_clamp_binds():
+    # amax/127 = 1.4 * 2^-24 rounds to the fp16 subnormal 2^-24, so amax / s16 = 177.8 and the
+    # definition's clamp to [-127, 127] decides the code of the largest element.
+    s_true = np.float32(1.4 * 2.0 ** -24)
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = s_true * np.float32(127.0)
+    x[0, 1] = -x[0, 0]
+    x[0, 2] = np.float32(2.0 ** -24) * np.float32(50.0)
+    q, s = keys.quantize_q8_0(x)
+    assert float(s[0, 0]) == 2.0 ** -24
+    assert q[0, 0] == 127 and q[0, 1] == -127 and q[0, 2] == 50
