@@ -39,7 +39,6 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
-#include <cuda.h>
 
 #include "polykv_internal.cuh"
 #include "tc_ptx.cuh"
@@ -51,21 +50,21 @@ constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kNR = 64;            // padded rows (MMA N)
 constexpr int kThreadsTc = 448;
-constexpr int kNS = 4;             // pool-tile ring depth
+constexpr int kNS = 8;             // pool-tile ring depth
 constexpr float kTau = 6.0f;       // lazy rescale threshold (log2 units)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kLog2eTc = 1.4426950408889634f;
 
-// one ring stage: key codes (swizzled) | scales | value codes | norms
-constexpr uint32_t kRawK = 0, kRawS = 16384, kRawV = 17408, kRawN = 23552;
-constexpr uint32_t kRawBytes = 23808;      // bytes delivered per tile
-constexpr uint32_t kRawStage = 24576;      // stage stride (keeps key tiles 1024-aligned)
+// one ring stage: block scales | value codes | norms (the key codes go straight to registers)
+constexpr uint32_t kRawS = 0, kRawV = 1024, kRawN = 7168;
+constexpr uint32_t kRawBytes = 7424;       // bytes delivered per tile
+constexpr uint32_t kRawStage = 7424;
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t kSmQ = 0;                            // 2 chunks x [64 rows][128 B]          16 KB
 constexpr uint32_t kSmV = kSmQ + 16384;                 // 2 stages x 2 dim blocks x [128][128 B] 64 KB
 constexpr uint32_t kSmP = kSmV + 65536;                 // 2 stages x [128 tokens][128 B]       32 KB
-constexpr uint32_t kSmRaw = kSmP + 32768;               // kNS x 24 KB                          96 KB
+constexpr uint32_t kSmRaw = kSmP + 32768;               // kNS x 7.25 KB                        58 KB
 constexpr uint32_t kSmLut = kSmRaw + kNS * kRawStage;   // 64 code pairs x 32 lanes x 4 B         8 KB
 constexpr uint32_t kSmMisc = kSmLut + 8192;
 constexpr uint32_t kSmBytes = kSmMisc + 2048 + 1024;    // + alignment slack
@@ -232,7 +231,7 @@ __device__ __noinline__ void softmax_rescale(Misc& M, int grp, int wq, int tt, i
 
 template <bool QBF16>
 __global__ void __launch_bounds__(kThreadsTc, 1)
-    attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams P) {
+    attend_tc_kernel(const TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u = tc::smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
@@ -305,7 +304,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 const uint32_t dst = tc::smem_u32(sR + st * kRawStage);
                 const uint32_t bar = tc::smem_u32(&M.rfull[st]);
                 tc::mbar_arrive_expect_tx(bar, kRawBytes);
-                tc::tma_2d_g2s(dst + kRawK, &kmap, 0, (int32_t)row0, bar);
                 tc::bulk_g2s(dst + kRawS, P.p.ks + row0 * (kD / kQ8Block), 1024, bar);
                 tc::bulk_g2s(dst + kRawV, P.p.vc + row0 * (3 * kD / 8), 6144, bar);
                 tc::bulk_g2s(dst + kRawN, P.p.vn + row0, 256, bar);
@@ -321,16 +319,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // =============================== producers
         const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
         const uint32_t t = (uint32_t)tid;
-        int ti_next = (int)(g0 % nt);
+        // key rows are read straight from HBM into registers one tile ahead (8 x 16 B per token)
+        int64_t u_n = g0 / nt;
+        int ti_n = (int)(g0 - u_n * nt);
+        uint4 kn[8];
+        auto fetch_k = [&](int64_t uu, int tti) {
+            const int64_t tok = (int64_t)tti * kTile + t;
+            const uint4* src = reinterpret_cast<const uint4*>(P.p.kq + (uu * cap + tok) * kD);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) kn[i] = tok < P.n_ctx ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        };
+        if (n > 0) fetch_k(u_n, ti_n);
         for (int j = 0; j < (int)n && !*abortp; ++j) {
-            const int ti = ti_next;
-            if (++ti_next == nt) ti_next = 0;
+            const int ti = ti_n;
+            if (++ti_n == nt) {
+                ti_n = 0;
+                ++u_n;
+            }
             const int s = j & 1;
             const uint32_t ph = (uint32_t)((j >> 1) & 1);
             const int st = j & (kNS - 1);
             const bool valid = (int64_t)ti * kTile + t < P.n_ctx;
-            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
-            const uint8_t* raw = sR + st * kRawStage;
             // keys: int8 codes -> fp16 -> TMEM lane = token
             if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.kfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
 #pragma unroll
@@ -338,8 +347,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 uint32_t r[16];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint4 kr = make_uint4(0u, 0u, 0u, 0u);
-                    if (valid) kr = *reinterpret_cast<const uint4*>(raw + kRawK + tc::sw128(t, (2 * qq + h) * 16));
+                    const uint4 kr = kn[2 * qq + h];
                     i8x4_to_f16x4(kr.x, r[h * 8 + 0], r[h * 8 + 1]);
                     i8x4_to_f16x4(kr.y, r[h * 8 + 2], r[h * 8 + 3]);
                     i8x4_to_f16x4(kr.z, r[h * 8 + 4], r[h * 8 + 5]);
@@ -350,6 +358,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::wait_st();
             tc::fence_before();
             tc::mbar_arrive(tc::smem_u32(&M.kfull[s]));
+            if (j + 1 < (int)n) fetch_k(u_n, ti_n);  // next tile's key rows, in flight during the value work
+            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
+            const uint8_t* raw = sR + st * kRawStage;
             // values: packed 3-bit codes -> fp16 centroids, token-major rows (MN-major A operand)
             if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
             uint32_t w[12];
@@ -534,20 +545,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
                 softmax_rescale(M, grp, wq, tt, rbase, gbar, first, j, lane_addr, abortp);
             }
-            // -------- probabilities, running sums, P' = p * ||v|| * wscale (fp16)
-            uint32_t pk[16];
+            // -------- probabilities, running sums, P' = p * ||v|| * wscale (fp16), stored as produced
+            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
+            uint8_t* prow = sP + s * 16384;
             const float2 wt2 = make_float2(wt, wt);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t tl[16];
                 if (!first) tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
 #pragma unroll
-                for (int k = 8 * cc; k < 8 * cc + 8; ++k) {
-                    const float2 d = sub2(x2[k], msm2[k]);
-                    x2[k] = make_float2(ex2(d.x), ex2(d.y));    // x2 now holds p
-                    const float2 pw = mul2(x2[k], wt2);
-                    const __half2 h = __floats2half2_rn(pw.x, pw.y);
-                    pk[k] = *reinterpret_cast<const uint32_t*>(&h);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 8 * cc + 4 * half + e;
+                        const float2 d = sub2(x2[k], msm2[k]);
+                        x2[k] = make_float2(ex2(d.x), ex2(d.y));  // x2 now holds p
+                        const float2 pw = mul2(x2[k], wt2);
+                        const __half2 h = __floats2half2_rn(pw.x, pw.y);
+                        pk[e] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    *reinterpret_cast<uint4*>(prow + tc::sw128((uint32_t)tt, 16u * (4 * grp + 2 * cc + half))) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 if (!first) tc::wait_ld();
 #pragma unroll
@@ -561,12 +580,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
                 tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
             }
-            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
-            uint8_t* prow = sP + s * 16384;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<uint4*>(prow + tc::sw128((uint32_t)tt, 16u * (4 * grp + cc))) =
-                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             tc::fence_proxy_async();
             tc::fence_before();
             tc::mbar_arrive(tc::smem_u32(&M.pfull[s]));
@@ -622,8 +635,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         auto issue_mma2 = [&](int jj, bool seg_first) -> bool {
             const int s2 = jj & 1;
             const uint32_t ph2 = (uint32_t)((jj >> 1) & 1);
-            if (!tc::mbar_wait(tc::smem_u32(&M.vfull[s2]), ph2, abortp, kTimeoutNs)) return false;
-            if (!tc::mbar_wait(tc::smem_u32(&M.pfull[s2]), ph2, abortp, kTimeoutNs)) return false;
+            if (!tc::mbar_wait(tc::smem_u32(&M.vfull[s2]), ph2, abortp, kTimeoutNs, false)) return false;
+            if (!tc::mbar_wait(tc::smem_u32(&M.pfull[s2]), ph2, abortp, kTimeoutNs, false)) return false;
             tc::fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -646,10 +659,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (first) {
                 if (j > 0 && !issue_mma2(j - 1, prev_first)) break;
                 ++seg;
-                if (!tc::mbar_wait(tc::smem_u32(&M.qready), (uint32_t)(seg & 1), abortp, kTimeoutNs)) break;
+                if (!tc::mbar_wait(tc::smem_u32(&M.qready), (uint32_t)(seg & 1), abortp, kTimeoutNs, false)) break;
             }
-            if (!tc::mbar_wait(tc::smem_u32(&M.kfull[s]), ph, abortp, kTimeoutNs)) break;
-            if (j > 0 && !tc::mbar_wait(tc::smem_u32(&M.sfree), (uint32_t)((j - 1) & 1), abortp, kTimeoutNs)) break;
+            if (!tc::mbar_wait(tc::smem_u32(&M.kfull[s]), ph, abortp, kTimeoutNs, false)) break;
+            if (j > 0 && !tc::mbar_wait(tc::smem_u32(&M.sfree), (uint32_t)((j - 1) & 1), abortp, kTimeoutNs, false)) break;
             tc::fence_after();
 #pragma unroll
             for (int b = 0; b < 4; ++b)
@@ -718,23 +731,6 @@ TcPlan plan(const PoolView& p, int64_t n_ctx) {
     return pl;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled_fn() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(ptr);
-    }();
-    return fn;
-}
-
 }  // namespace
 
 bool attend_tc_supported(const PoolView& p, int rows) { return p.d == kD && rows >= 1 && rows <= kNR; }
@@ -754,19 +750,7 @@ polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q
     const TcPlan pl = plan(p, n_ctx);
     const size_t need = attend_tc_workspace(p, R, n_ctx);
     if (ws_bytes < need) return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend: workspace %zu < %zu bytes", ws_bytes, need);
-    // key codes as a 2-D [U*cap rows][128 bytes] tensor, 128-row boxes, 128B swizzle
-    const EncodeTiledFn enc = encode_tiled_fn();
-    if (!enc) return set_error(POLYKV_E_CUDA, "attend_tc: cuTensorMapEncodeTiled unavailable");
-    CUtensorMap kmap;
     const size_t U = (size_t)p.L * p.H;
-    const cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)(U * (size_t)p.cap)};
-    const cuuint64_t gstride[1] = {(cuuint64_t)kD};
-    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kTile};
-    const cuuint32_t estride[2] = {1, 1};
-    const CUresult cr = enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)p.kq, gdim, gstride, box, estride,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return set_error(POLYKV_E_CUDA, "attend_tc: tensor map encode failed (%d)", (int)cr);
     TcParams P;
     P.p = p;
     P.q = static_cast<const uint16_t*>(q);
@@ -789,7 +773,7 @@ polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q
     auto kern = dt == POLYKV_BF16 ? attend_tc_kernel<true> : attend_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmBytes);
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_tc: smem attribute: %s", cudaGetErrorString(e));
-    kern<<<pl.nctas, kThreadsTc, kSmBytes, stream>>>(kmap, P);
+    kern<<<pl.nctas, kThreadsTc, kSmBytes, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_tc launch: %s", cudaGetErrorString(e));
     return launch_attend_merge(P.ws_acc, P.ws_ml, out, (int)U, p.H, n_agents, n_q_heads, R, pl.pmax, pl.nt, pl.tt,

@@ -94,17 +94,23 @@ __device__ __forceinline__ void unpack32(const uint4 (&raw)[4], float (&x)[32], 
     }
 }
 
-__device__ __forceinline__ uint32_t ge_mask(float a, float b) {
+__device__ __forceinline__ uint32_t ge_mask_s32(int32_t a, int32_t b) {
     uint32_t m;  // 0xFFFFFFFF if a >= b else 0
-    asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
+    asm("set.ge.u32.s32 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
     return m;
 }
 
+// code = number of boundaries b_i <= u, on the float bits: the boundaries are symmetric
+// (b_{6-i} = -b_i, b_3 = 0), positive floats order like their bit patterns, and for u < 0
+// "u >= -b" is "|u| <= b", i.e. not "|u| > b" -- taking one off |u|'s bits turns the strict
+// comparison into >=. (u = -0 cannot reach here: it needs ||v|| = 0, which is encoded as +0.)
 __device__ __forceinline__ uint32_t value_code(float u) {
-    // number of boundaries b_i <= u (boundaries symmetric about 0): minus the sum of seven masks
-    const uint32_t s = ge_mask(u, -kB6) + ge_mask(u, -kB5) + ge_mask(u, -kB4) + ge_mask(u, 0.0f) + ge_mask(u, kB4) +
-                       ge_mask(u, kB5) + ge_mask(u, kB6);
-    return 0u - s;
+    const int32_t bits = __float_as_int(u);
+    const int32_t sm = bits >> 31;                   // -1 for u < 0, else 0
+    const int32_t t = (bits & 0x7FFFFFFF) + sm;
+    const uint32_t neg_count = ge_mask_s32(t, __float_as_int(kB4)) + ge_mask_s32(t, __float_as_int(kB5)) +
+                               ge_mask_s32(t, __float_as_int(kB6));   // minus the number passed
+    return (4u - neg_count) ^ ((uint32_t)sm & 7u);
 }
 
 __device__ __forceinline__ uint32_t bytes4(int a, int b, int c, int d) {

@@ -115,11 +115,12 @@ __device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity, 
 
 // Wait for the phase with `parity` to complete, giving up after ~timeout_ns.
 // On give-up (or if another role already gave up) it sets *abort and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns,
+                                          bool suspend = true) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
-        if (mbar_try_suspend(bar, parity, 2000u)) return true;
+        if (suspend ? mbar_try_suspend(bar, parity, 2000u) : mbar_try(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer() - t0 > timeout_ns) {
             *abort = 1;
