@@ -71,8 +71,8 @@ constexpr uint32_t kSmBytes = kSmMisc + 2048 + 1024;    // + alignment slack
 static_assert(kSmBytes <= 232448, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t kColK = 0;     // 2 stages x 64
-constexpr uint32_t kColS = 128;   // 4 blocks x 64
+constexpr uint32_t kColK = 0;     // 2 stages x (64 hi + 64 lo)
+constexpr uint32_t kColS = 256;   // 2 buffers x 64
 constexpr uint32_t kColO = 384;   // 64
 constexpr uint32_t kColL = 448;   // 64: per-token-slot partial row sums (lane = token slot)
 constexpr uint32_t kTmemCols = 512;
@@ -102,7 +102,7 @@ struct Misc {
     int flags[2][3];
     int abort;
     int pad;
-    uint64_t kfull[2], kfree[2], vfull[2], pfull[2], pvfree[2], sfull, sfree, qready, done;
+    uint64_t kfull[2], kfree[2], vfull[2], pfull[2], pvfree[2], sfull[2], sfree[2], qready, done;
     uint64_t rfull[kNS], rempty[kNS];
     uint32_t tslot;
 };
@@ -172,21 +172,24 @@ __device__ __forceinline__ uint32_t code_pair(const uint32_t (&w)[12]) {
     }
 }
 
+// Four 16-byte chunks (dims 8C..8C+31) of one token's fp16 centroid row: all sixteen
+// code-pair lookups are issued before the four stores, so their latencies overlap.
 template <int C>
-__device__ __forceinline__ void store_v_chunks(const uint32_t (&w)[12], const uint32_t* lut, uint8_t* vstage,
-                                               uint32_t tok, bool valid) {
-    if constexpr (C < 16) {
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) {
-            o.x = lut[code_pair<4 * C + 0>(w) * 32];
-            o.y = lut[code_pair<4 * C + 1>(w) * 32];
-            o.z = lut[code_pair<4 * C + 2>(w) * 32];
-            o.w = lut[code_pair<4 * C + 3>(w) * 32];
-        }
-        // dims 8C..8C+7 -> dim block C/8, chunk C%8 of this token's 128-byte row
-        *reinterpret_cast<uint4*>(vstage + (C / 8) * 16384 + tc::sw128(tok, (C % 8) * 16)) = o;
-        store_v_chunks<C + 1>(w, lut, vstage, tok, valid);
+__device__ __forceinline__ void store_v_quad(const uint32_t (&w)[12], const uint32_t* __restrict__ lut,
+                                             uint8_t* __restrict__ vstage, uint32_t tok, bool valid) {
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i] = 0u;
+    if (valid) {
+#define PKV_LUT(I) o[I] = lut[code_pair<4 * C + I>(w) * 32];
+        PKV_LUT(0) PKV_LUT(1) PKV_LUT(2) PKV_LUT(3) PKV_LUT(4) PKV_LUT(5) PKV_LUT(6) PKV_LUT(7)
+        PKV_LUT(8) PKV_LUT(9) PKV_LUT(10) PKV_LUT(11) PKV_LUT(12) PKV_LUT(13) PKV_LUT(14) PKV_LUT(15)
+#undef PKV_LUT
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(vstage + ((C + q) / 8) * 16384 + tc::sw128(tok, ((C + q) % 8) * 16)) =
+            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
 }
 
 // Lazy-rescale path of the softmax (rare): with the tile's per-warp row maxima in
@@ -265,8 +268,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::mbar_init(tc::smem_u32(&M.rfull[s]), 1);
             tc::mbar_init(tc::smem_u32(&M.rempty[s]), 128 + 256);
         }
-        tc::mbar_init(tc::smem_u32(&M.sfull), 1);
-        tc::mbar_init(tc::smem_u32(&M.sfree), 256);
+        for (int s2 = 0; s2 < 2; ++s2) {
+            tc::mbar_init(tc::smem_u32(&M.sfull[s2]), 1);
+            tc::mbar_init(tc::smem_u32(&M.sfree[s2]), 256);
+        }
         tc::mbar_init(tc::smem_u32(&M.qready), 1);
         tc::mbar_init(tc::smem_u32(&M.done), 1);
         M.abort = 0;
@@ -340,27 +345,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint32_t ph = (uint32_t)((j >> 1) & 1);
             const int st = j & (kNS - 1);
             const bool valid = (int64_t)ti * kTile + t < P.n_ctx;
-            // keys: int8 codes -> fp16 -> TMEM lane = token
+            // keys: k_hat = s_b * code (times 2^-4 against fp16 overflow) as an exact fp16 pair
+            // hi = fp16(k_hat), lo = fp16(k_hat - hi): the product has <= 18 significant bits, hi + lo
+            // holds 22, so hi + lo = k_hat and MMA1 over hi then lo gives the exact q . k_hat sums.
+            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
+            const uint8_t* raw = sR + st * kRawStage;
+            const uint2 sraw = valid ? *reinterpret_cast<const uint2*>(raw + kRawS + t * 8) : make_uint2(0u, 0u);
             if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.kfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                uint32_t r[16];
+            for (int qq = 0; qq < 4; ++qq) {   // q8_0 block qq = dims 32qq .. 32qq+31
+                const uint32_t sw = (qq < 2 ? sraw.x : sraw.y) >> (16 * (qq & 1));
+                __half2 sc = __half2half2(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
+                sc = __hmul2(sc, __half2half2(__ushort_as_half((unsigned short)0x2C00)));  // * 2^-4
+                uint32_t rh[16], rl[16];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint4 kr = kn[2 * qq + h];
-                    i8x4_to_f16x4(kr.x, r[h * 8 + 0], r[h * 8 + 1]);
-                    i8x4_to_f16x4(kr.y, r[h * 8 + 2], r[h * 8 + 3]);
-                    i8x4_to_f16x4(kr.z, r[h * 8 + 4], r[h * 8 + 5]);
-                    i8x4_to_f16x4(kr.w, r[h * 8 + 6], r[h * 8 + 7]);
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t c01, c23;
+                        i8x4_to_f16x4(valid ? kw[e] : 0u, c01, c23);
+                        const __half2 h01 = __hmul2(*reinterpret_cast<const __half2*>(&c01), sc);
+                        const __half2 h23 = __hmul2(*reinterpret_cast<const __half2*>(&c23), sc);
+                        const __half2 l01 = __hfma2(*reinterpret_cast<const __half2*>(&c01), sc, __hneg2(h01));
+                        const __half2 l23 = __hfma2(*reinterpret_cast<const __half2*>(&c23), sc, __hneg2(h23));
+                        rh[h * 8 + 2 * e] = *reinterpret_cast<const uint32_t*>(&h01);
+                        rh[h * 8 + 2 * e + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+                        rl[h * 8 + 2 * e] = *reinterpret_cast<const uint32_t*>(&l01);
+                        rl[h * 8 + 2 * e + 1] = *reinterpret_cast<const uint32_t*>(&l23);
+                    }
                 }
-                tc::tmem_st16(lane_addr + kColK + 64u * s + 16u * qq, r);
+                tc::tmem_st16(lane_addr + kColK + 128u * s + 16u * qq, rh);
+                tc::tmem_st16(lane_addr + kColK + 128u * s + 64u + 16u * qq, rl);
             }
             tc::wait_st();
             tc::fence_before();
             tc::mbar_arrive(tc::smem_u32(&M.kfull[s]));
             if (j + 1 < (int)n) fetch_k(u_n, ti_n);  // next tile's key rows, in flight during the value work
-            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
-            const uint8_t* raw = sR + st * kRawStage;
             // values: packed 3-bit codes -> fp16 centroids, token-major rows (MN-major A operand)
             if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
             uint32_t w[12];
@@ -373,7 +395,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 w[4 * i + 3] = x.w;
             }
             tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
-            store_v_chunks<0>(w, lut + lane, sV + s * 32768, t, valid);
+            store_v_quad<0>(w, lut + lane, sV + s * 32768, t, valid);
+            store_v_quad<4>(w, lut + lane, sV + s * 32768, t, valid);
+            store_v_quad<8>(w, lut + lane, sV + s * 32768, t, valid);
+            store_v_quad<12>(w, lut + lane, sV + s * 32768, t, valid);
             tc::fence_proxy_async();
             tc::mbar_arrive(tc::smem_u32(&M.vfull[s]));
         }
@@ -475,7 +500,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     const float nmax = P.p.nmax[u];
                     int en = 0;
                     if (nmax > 0.0f) frexpf(nmax, &en);
-                    M.scale_eff = P.scale_log2 / fq;
+                    M.scale_eff = P.scale_log2 * 16.0f / fq;  // keys are stored in TMEM as s * code * 2^-4
                     M.wscale = nmax > 0.0f ? ldexpf(1.0f, 8 - en) : 1.0f;  // ||v|| * wscale < 2^8
                 }
                 if (si < kNR) M.msm[si] = si < R ? -INFINITY : INFINITY;
@@ -487,38 +512,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const float wscale = M.wscale;
             const int64_t tok = (int64_t)ti * kTile + tt;
             const bool valid = tok < P.n_ctx;
-            // per-token block scales and norm from the ring (after an abort the waits return at once and the
-            // loop runs to the end with garbage, so both row groups pass the same named barriers)
+            // per-token norm from the ring (after an abort the waits return at once and the loop runs to the
+            // end with garbage, so both row groups pass the same named barriers)
             tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs);
-            const uint8_t* raw = sR + st * kRawStage;
-            const uint2 sr = *reinterpret_cast<const uint2*>(raw + kRawS + tt * 8);
-            const unsigned short nb = *reinterpret_cast<const unsigned short*>(raw + kRawN + tt * 2);
+            const unsigned short nb = *reinterpret_cast<const unsigned short*>(sR + st * kRawStage + kRawN + tt * 2);
             tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
-            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sr.x));
-            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sr.y));
-            const float sb[4] = {s01.x * scale_eff, s01.y * scale_eff, s23.x * scale_eff, s23.y * scale_eff};
             const float wt = valid ? __half2float(__ushort_as_half(nb)) * wscale : 0.0f;
-            // -------- logits from the four block accumulators (this group's 32 rows)
+            // -------- logits: x = scale_eff * (q' . k_hat) for this group's 32 rows
             float2 x2[16];
-            tc::mbar_wait(tc::smem_u32(&M.sfull), (uint32_t)(j & 1), abortp, kTimeoutNs);
+            tc::mbar_wait(tc::smem_u32(&M.sfull[s]), ph, abortp, kTimeoutNs);
             tc::fence_after();
+            {
+                uint32_t t0[16], t1[16];
+                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase, t0);
+                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase + 16u, t1);
+                tc::wait_ld();
+                const float2 c2 = make_float2(scale_eff, scale_eff);
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const float2 sb2 = make_float2(sb[b], sb[b]);
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t t0[16];
-                    tc::tmem_ld16(lane_addr + kColS + 64u * b + rbase + 16u * cc, t0);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float2 a0 = make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1]));
-                        x2[8 * cc + k] = b == 0 ? mul2(sb2, a0) : fma2(sb2, a0, x2[8 * cc + k]);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    x2[k] = mul2(c2, make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1])));
+                    x2[8 + k] = mul2(c2, make_float2(__uint_as_float(t1[2 * k]), __uint_as_float(t1[2 * k + 1])));
                 }
             }
             tc::fence_before();
-            tc::mbar_arrive(tc::smem_u32(&M.sfree));
+            tc::mbar_arrive(tc::smem_u32(&M.sfree[s]));
             if (!valid) {
 #pragma unroll
                 for (int k = 0; k < 16; ++k) x2[k] = make_float2(-INFINITY, -INFINITY);
@@ -662,17 +679,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 if (!tc::mbar_wait(tc::smem_u32(&M.qready), (uint32_t)(seg & 1), abortp, kTimeoutNs, false)) break;
             }
             if (!tc::mbar_wait(tc::smem_u32(&M.kfull[s]), ph, abortp, kTimeoutNs, false)) break;
-            if (j > 0 && !tc::mbar_wait(tc::smem_u32(&M.sfree), (uint32_t)((j - 1) & 1), abortp, kTimeoutNs, false)) break;
+            if (j >= 2 &&
+                !tc::mbar_wait(tc::smem_u32(&M.sfree[s]), (uint32_t)(((j - 2) >> 1) & 1), abortp, kTimeoutNs, false))
+                break;
             tc::fence_after();
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+            for (int part = 0; part < 2; ++part)   // hi then lo halves of the scaled keys
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const int ks = 2 * b + kk;
+                for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t bd = tc::sdesc(sq + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
-                    tc::mma_ts(tbase + kColS + 64u * b, tbase + kColK + 64u * s + 8u * ks, bd, id1, (uint32_t)kk);
+                    tc::mma_ts(tbase + kColS + 64u * s, tbase + kColK + 128u * s + 64u * part + 8u * ks, bd, id1,
+                               (part | ks) ? 1u : 0u);
                 }
-            tc::commit(tc::smem_u32(&M.sfull));
+            tc::commit(tc::smem_u32(&M.sfull[s]));
             tc::commit(tc::smem_u32(&M.kfree[s]));
             if (!first) ok = issue_mma2(j - 1, prev_first);
             prev_first = first;
