@@ -152,6 +152,23 @@ POLYKV_API polykv_status polykv_attend(const polykv_pool* pool, const void* q, f
                             int32_t n_q_heads, int64_t n_ctx, float softmax_scale, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* polykv_attend without a caller workspace (an addition of this library; the paper has no
+ * counterpart). For callers that cannot allocate device memory when they attend -- code running
+ * while a CUDA graph is captured elsewhere in the process, embeddings without an allocator, or
+ * hosts with a fixed memory budget -- the split partials go to a 16 MiB array that is part of the
+ * library's device module (held on every GPU that loads the library until the process exits).
+ * Arguments and output are those of polykv_attend; nothing is allocated. Arguments that would
+ * need more than 16 MiB of partials return POLYKV_E_BUFFER_TOO_SMALL with a message (the
+ * Llama-3-8B shape with 15 agents needs about 16.0 MB on a 152-SM GB300).
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture. All calls share the one array:
+ * calls that may overlap on the GPU (other streams, other host threads) race on it and must be
+ * ordered by the caller. The array keeps the last call's partials; every call writes each slot it
+ * reads, so nothing needs clearing between calls. */
+POLYKV_API polykv_status polykv_attend_static_ws(const polykv_pool* pool, const void* q, float* out,
+                                                 int32_t n_agents, int32_t n_q_heads, int64_t n_ctx,
+                                                 float softmax_scale, void* stream);
+
 /* Read and clear the pool's device status word (synchronises `stream`).
  * Bit 0: a kernel gave up on a bounded device-side wait (about 2 s) and its
  * results are invalid; the call then returns POLYKV_E_TIMEOUT. *flags gets the

@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "polykv_free": [vp],
         "polykv_codebook": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
         "polykv_pool_status": [vp, vp, ctypes.POINTER(ctypes.c_uint32)],
+        "polykv_attend_static_ws": [vp, vp, vp, i32, i32, i64, f32, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -111,6 +112,14 @@ def polykv_attend(handle: int, q_ptr: int, out_ptr: int, n_agents: int, n_q_head
                   softmax_scale: float, ws_ptr: int | None, ws_bytes: int, stream: int | None):
     _check(load_library().polykv_attend(handle, q_ptr, out_ptr, n_agents, n_q_heads, n_ctx, softmax_scale, ws_ptr,
                                         ws_bytes, stream))
+
+
+def polykv_attend_static_ws(handle: int, q_ptr: int, out_ptr: int, n_agents: int, n_q_heads: int, n_ctx: int,
+                            softmax_scale: float, stream: int | None):
+    """polykv_attend with the library's built-in 16 MiB partials array instead of a caller
+    workspace (for callers that cannot allocate device memory when they attend)."""
+    _check(load_library().polykv_attend_static_ws(handle, q_ptr, out_ptr, n_agents, n_q_heads, n_ctx,
+                                                  softmax_scale, stream))
 
 
 def polykv_pool_status(handle: int, stream: int | None) -> int:

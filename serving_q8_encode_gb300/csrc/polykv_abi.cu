@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "polykv_internal.cuh"
@@ -193,6 +194,67 @@ polykv_status polykv_attend(const polykv_pool* pool, const void* q, float* out, 
                                 workspace_bytes, static_cast<cudaStream_t>(stream));
     return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
                               workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Attention without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run attention: code that
+// runs while a CUDA graph is being captured elsewhere in the process, allocator-less embedding
+// layers, or hosts whose memory budget is fixed up front. For them the split partials live in a
+// file-scope device array instead. The array is part of the library's module, so every GPU that
+// loads the library holds it until the process exits; its size is therefore kept modest and
+// fixed: 16 MiB, enough for the Llama-3-8B shape (32 layers x 8 kv heads, 15 agents x 4 query
+// heads, any context length on a 152-SM GB300).
+namespace polykv {
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
+static __device__ __align__(256) unsigned char g_attend_scratch[kStaticScratchBytes];
+static void* g_scratch_dev_ptr[128] = {nullptr};
+static std::mutex g_scratch_mu;
+
+// Device address of the scratch array for the current device. Host code only sees a host-side
+// stand-in for the symbol, so the address is looked up once per device (the first call on a
+// device) and cached.
+static polykv_status static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_static: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 128) return set_error(POLYKV_E_UNSUPPORTED, "attend_static: device %d", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_dev_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attend_scratch);
+        if (e != cudaSuccess || !p)
+            return set_error(POLYKV_E_CUDA, "attend_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_scratch_dev_ptr[dev] = p;
+    }
+    *out = g_scratch_dev_ptr[dev];
+    return POLYKV_OK;
+}
+}  // namespace polykv
+
+polykv_status polykv_attend_static_ws(const polykv_pool* pool, const void* q, float* out, int32_t n_agents,
+                                      int32_t n_q_heads, int64_t n_ctx, float softmax_scale, void* stream) {
+    const polykv_status st = check_attend_args(pool, n_agents, n_q_heads, n_ctx);
+    if (st != POLYKV_OK) return st;
+    if (!q || !out) return set_error(POLYKV_E_INVAL, "q and out must be non-NULL");
+    if (!aligned16(q) || !aligned16(out)) return set_error(POLYKV_E_INVAL, "q and out must be 16-byte aligned");
+    const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
+    const size_t need = attend_workspace(pool->view, rows, n_ctx);
+    if (need > kStaticScratchBytes)
+        return set_error(POLYKV_E_BUFFER_TOO_SMALL,
+                         "attend_static: these arguments need %zu bytes of scratch, the built-in array holds %zu; "
+                         "use polykv_attend with a caller workspace",
+                         need, kStaticScratchBytes);
+    void* ws = nullptr;
+    const polykv_status s2 = static_scratch(&ws);
+    if (s2 != POLYKV_OK) return s2;
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
+    if (use_tc_path(pool->view, rows))
+        return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, ws,
+                                kStaticScratchBytes, static_cast<cudaStream_t>(stream));
+    return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, ws,
+                              kStaticScratchBytes, static_cast<cudaStream_t>(stream));
 }
 
 polykv_status polykv_pool_status(const polykv_pool* pool, void* stream, uint32_t* flags) {
