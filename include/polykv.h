@@ -152,6 +152,31 @@ POLYKV_API polykv_status polykv_attend(const polykv_pool* pool, const void* q, f
                             int32_t n_q_heads, int64_t n_ctx, float softmax_scale, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* Extensions of an attend call (zero-initialise and set what is used). */
+typedef struct {
+    /* Private per-agent suffix: each agent's own uncompressed recent tokens, attended together with
+     * the pool under ONE softmax. in_dtype bits, [n_layers][n_agents][n_kv_heads][suffix_len][head_dim]
+     * contiguous, device, 16-byte aligned. suffix_len = 0 disables it. At most 16 query heads per
+     * kv head. */
+    const void* suffix_k;
+    const void* suffix_v;
+    int64_t suffix_len;
+} polykv_attend_ext;
+
+/* Workspace bytes for polykv_attend_ex with these arguments (ext may be NULL). */
+POLYKV_API polykv_status polykv_attend_ex_workspace_size(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads,
+                                                         int64_t n_ctx, const polykv_attend_ext* ext, size_t* bytes);
+
+/* polykv_attend with extensions. With a suffix the output is
+ *   out[l][a][hq] = sum over pool tokens t < n_ctx and suffix tokens s of softmax(scale * q.k) v
+ * where pool keys/values are dequantized as in polykv_attend and suffix keys/values are used as
+ * given. Errors as polykv_attend, plus E_INVAL for a bad suffix and E_UNSUPPORTED for more than 16
+ * query heads per kv head. ext may be NULL (then identical to polykv_attend). */
+POLYKV_API polykv_status polykv_attend_ex(const polykv_pool* pool, const void* q, float* out, int32_t n_agents,
+                                          int32_t n_q_heads, int64_t n_ctx, float softmax_scale,
+                                          const polykv_attend_ext* ext, void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
 /* polykv_attend without a caller workspace (an addition of this library; the paper has no
  * counterpart). For callers that cannot allocate device memory when they attend -- code running
  * while a CUDA graph is captured elsewhere in the process, embeddings without an allocator, or

@@ -42,6 +42,10 @@ class PoolRegions(ctypes.Structure):
                 ("header_bytes", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
 
 
+class AttendExt(ctypes.Structure):
+    _fields_ = [("suffix_k", ctypes.c_void_p), ("suffix_v", ctypes.c_void_p), ("suffix_len", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -65,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "polykv_codebook": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
         "polykv_pool_status": [vp, vp, ctypes.POINTER(ctypes.c_uint32)],
         "polykv_attend_static_ws": [vp, vp, vp, i32, i32, i64, f32, vp],
+        "polykv_attend_ex_workspace_size": [vp, i32, i32, i64, ctypes.POINTER(AttendExt), ctypes.POINTER(sz)],
+        "polykv_attend_ex": [vp, vp, vp, i32, i32, i64, f32, ctypes.POINTER(AttendExt), vp, sz, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -127,6 +133,22 @@ def polykv_pool_status(handle: int, stream: int | None) -> int:
     f = ctypes.c_uint32()
     _check(load_library().polykv_pool_status(handle, stream, ctypes.byref(f)))
     return f.value
+
+
+def polykv_attend_ex_workspace_size(handle: int, n_agents: int, n_q_heads: int, n_ctx: int,
+                                    ext: AttendExt | None) -> int:
+    b = ctypes.c_size_t()
+    _check(load_library().polykv_attend_ex_workspace_size(handle, n_agents, n_q_heads, n_ctx,
+                                                          ctypes.byref(ext) if ext is not None else None,
+                                                          ctypes.byref(b)))
+    return b.value
+
+
+def polykv_attend_ex(handle: int, q_ptr: int, out_ptr: int, n_agents: int, n_q_heads: int, n_ctx: int,
+                     softmax_scale: float, ext: AttendExt | None, ws_ptr: int | None, ws_bytes: int,
+                     stream: int | None):
+    _check(load_library().polykv_attend_ex(handle, q_ptr, out_ptr, n_agents, n_q_heads, n_ctx, softmax_scale,
+                                           ctypes.byref(ext) if ext is not None else None, ws_ptr, ws_bytes, stream))
 
 
 def polykv_free(handle: int | None):
@@ -205,6 +227,22 @@ class Pool:
             workspace = self._ws
         polykv_attend(self.handle, q.data_ptr(), out.data_ptr(), A, Hq, n_ctx, softmax_scale,
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        return out
+
+    def attend_with_suffix(self, q, n_ctx: int, suffix_k, suffix_v, out=None, softmax_scale: float = 0.0,
+                           stream=None):
+        """Pool plus each agent's private uncompressed suffix under one softmax.
+        suffix_k/v: device [L][A][H][S][d] (pool dtype bits), contiguous."""
+        import torch
+        L, A, Hq, d = q.shape
+        assert suffix_k.is_contiguous() and suffix_v.is_contiguous() and suffix_k.shape == suffix_v.shape
+        ext = AttendExt(suffix_k.data_ptr(), suffix_v.data_ptr(), suffix_k.shape[3])
+        if out is None:
+            out = torch.empty((L, A, Hq, d), dtype=torch.float32, device=q.device)
+        need = polykv_attend_ex_workspace_size(self.handle, A, Hq, n_ctx, ext)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        polykv_attend_ex(self.handle, q.data_ptr(), out.data_ptr(), A, Hq, n_ctx, softmax_scale, ext, ws.data_ptr(),
+                         ws.numel(), _stream_handle(stream))
         return out
 
     # -- views of the encoded fields (for inspection and tests)

@@ -273,7 +273,9 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
 template <int D>
 __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
                                                     float* __restrict__ out, int U, int H, int A, int Hq, int R,
-                                                    int n_slots, int64_t nt, int64_t tt, int nc) {
+                                                    int n_slots, int64_t nt, int64_t tt, int nc,
+                                                    const float* __restrict__ sfx_acc,
+                                                    const float* __restrict__ sfx_ml) {
     constexpr int EPL = D / 32;  // elements per lane
     const int wid = blockIdx.x * 4 + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -289,8 +291,10 @@ __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws
         const int64_t hi = (((int64_t)unit * nt + nt) * nc - 1) / tt;
         pieces = (int)(hi - lo + 1);
     }
+    const int64_t orow = ((int64_t)layer * A + a) * Hq + kvh * G + g;   // output / suffix row
     float M = -INFINITY;
     for (int s = 0; s < pieces; ++s) M = fmaxf(M, ws_ml[(((int64_t)unit * n_slots + s) * R + r) * 2]);
+    if (sfx_ml) M = fmaxf(M, sfx_ml[orow * 2]);
     float L = 0.0f;
     float o[EPL];
 #pragma unroll
@@ -305,9 +309,6 @@ __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, src[e], o[e]);
     }
-    const float inv = 1.0f / L;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] *= inv;
     // in-lane butterflies (strides < EPL), then across lanes
 #pragma unroll
     for (int h = 1; h < EPL; h <<= 1)
@@ -327,14 +328,29 @@ __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws
             o[e] = upper ? other - o[e] : o[e] + other;
         }
     }
-    float* dst = out + (((int64_t)layer * A + a) * Hq + kvh * G + g) * D + lane * EPL;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) dst[e] = o[e] * (1.0f / D);
+    for (int e = 0; e < EPL; ++e) o[e] *= (1.0f / D);
+    if (sfx_ml) {
+        // the suffix partial is already in the original basis
+        const float ms = sfx_ml[orow * 2];
+        if (ms != -INFINITY) {
+            const float w = exp2f(ms - M);
+            L = fmaf(w, sfx_ml[orow * 2 + 1], L);
+            const float* src = sfx_acc + orow * D + lane * EPL;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, src[e], o[e]);
+        }
+    }
+    const float inv = 1.0f / L;
+    float* dst = out + orow * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dst[e] = o[e] * inv;
 }
 
 template <int D, int RMAX, bool BF16>
 polykv_status run_simt(const PoolView& p, const void* q, float* out, int A, int Hq, int R, int64_t n_ctx,
-                       float scale, float* ws, int n_splits, int64_t split_len, cudaStream_t st) {
+                       float scale, float* ws, int n_splits, int64_t split_len, cudaStream_t st,
+                       const SuffixArgs* sfx) {
     using S = SimtSmem<D, RMAX>;
     auto kern = attend_partial_simt<D, RMAX, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
@@ -347,16 +363,22 @@ polykv_status run_simt(const PoolView& p, const void* q, float* out, int A, int 
                                             scale * kLog2e, ws_acc, ws_ml);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend partial launch: %s", cudaGetErrorString(e));
-    return launch_attend_merge(ws_acc, ws_ml, out, U, p.H, A, Hq, R, n_splits, 0, 0, 0, D, st);
+    if (sfx) {
+        const polykv_status ss = launch_attend_suffix(*sfx, BF16 ? POLYKV_BF16 : POLYKV_F16, p.L, A, p.H, Hq, D, scale, st);
+        if (ss != POLYKV_OK) return ss;
+    }
+    return launch_attend_merge(ws_acc, ws_ml, out, U, p.H, A, Hq, R, n_splits, 0, 0, 0, D, st,
+                               sfx ? sfx->acc : nullptr, sfx ? sfx->ml : nullptr);
 }
 
 template <int D, bool BF16>
 polykv_status dispatch_rows(const PoolView& p, const void* q, float* out, int A, int Hq, int R, int64_t n_ctx,
-                            float scale, float* ws, int n_splits, int64_t split_len, cudaStream_t st) {
-    if (R <= 8) return run_simt<D, 8, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
-    if (R <= 16) return run_simt<D, 16, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
-    if (R <= 32) return run_simt<D, 32, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
-    return run_simt<D, kMaxRowsPerCta, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st);
+                            float scale, float* ws, int n_splits, int64_t split_len, cudaStream_t st,
+                            const SuffixArgs* sfx) {
+    if (R <= 8) return run_simt<D, 8, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st, sfx);
+    if (R <= 16) return run_simt<D, 16, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st, sfx);
+    if (R <= 32) return run_simt<D, 32, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st, sfx);
+    return run_simt<D, kMaxRowsPerCta, BF16>(p, q, out, A, Hq, R, n_ctx, scale, ws, n_splits, split_len, st, sfx);
 }
 
 int64_t split_length(const PoolView& p, int rows, int64_t n_ctx) {
@@ -373,13 +395,16 @@ int64_t split_length(const PoolView& p, int rows, int64_t n_ctx) {
 }  // namespace
 
 polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float* out, int U, int H, int A, int Hq,
-                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st) {
+                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st,
+                                  const float* sfx_acc, const float* sfx_ml) {
     const int64_t warps = (int64_t)U * R;
     const unsigned blocks = (unsigned)((warps + 3) / 4);
     if (D == 128)
-        attend_merge<128><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc);
+        attend_merge<128><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc, sfx_acc,
+                                                  sfx_ml);
     else
-        attend_merge<64><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc);
+        attend_merge<64><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc, sfx_acc,
+                                                 sfx_ml);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend merge launch: %s", cudaGetErrorString(e));
     return POLYKV_OK;
@@ -398,7 +423,7 @@ size_t attend_simt_workspace(const PoolView& p, int rows, int64_t n_ctx) {
 
 polykv_status launch_attend_simt(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
                                  int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const SuffixArgs* sfx) {
     const int R = n_agents * (n_q_heads / p.H);
     const int64_t len = split_length(p, R, n_ctx);
     const int S = (int)((n_ctx + len - 1) / len);
@@ -408,11 +433,11 @@ polykv_status launch_attend_simt(const PoolView& p, polykv_dtype dt, const void*
     float* w = static_cast<float*>(ws);
     const bool bf = dt == POLYKV_BF16;
     if (p.d == 128)
-        return bf ? dispatch_rows<128, true>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream)
-                  : dispatch_rows<128, false>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream);
+        return bf ? dispatch_rows<128, true>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream, sfx)
+                  : dispatch_rows<128, false>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream, sfx);
     if (p.d == 64)
-        return bf ? dispatch_rows<64, true>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream)
-                  : dispatch_rows<64, false>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream);
+        return bf ? dispatch_rows<64, true>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream, sfx)
+                  : dispatch_rows<64, false>(p, q, out, n_agents, n_q_heads, R, n_ctx, scale, w, S, len, stream, sfx);
     return set_error(POLYKV_E_UNSUPPORTED, "attend: head_dim %d", p.d);
 }
 

@@ -1,0 +1,171 @@
+// Private per-agent suffix of uncompressed keys/values, attended together with
+// the shared compressed pool under ONE softmax.
+//
+// Each agent appends its own recent tokens after the shared context; those
+// are not part of the compressed pool (the PolyKV abstract's pool is the shared
+// context written once). For every (layer, agent, kv head) this kernel scores
+// the agent's G query heads against its suffix keys and accumulates the suffix
+// values in the ORIGINAL basis, producing one online-softmax partial (running
+// max m in log2 units, sum l, unnormalised accumulator) per query head. The
+// merge kernel combines it with the pool partials (whose accumulators are in
+// the rotated basis) after the pool part's inverse FWHT.
+#include <cmath>
+
+#include "polykv_internal.cuh"
+
+namespace polykv {
+namespace {
+
+constexpr int kSfxTile = 128;   // suffix tokens per tile (one per thread)
+constexpr int kSfxThreads = 128;
+
+__device__ __forceinline__ float bits_to_float(uint16_t b, bool bf16) {
+    return bf16 ? __uint_as_float((uint32_t)b << 16) : __half2float(__ushort_as_half(b));
+}
+
+// grid: one block per (layer, agent, kv head); block: 128 threads.
+template <int D, int GMAX, bool BF16>
+__global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __restrict__ q,
+                                                              const uint16_t* __restrict__ sk,
+                                                              const uint16_t* __restrict__ sv, int A, int H, int Hq,
+                                                              int64_t S, float scale_log2, float* __restrict__ acc_out,
+                                                              float* __restrict__ ml_out) {
+    __shared__ float qs[GMAX][D];
+    __shared__ float ps[GMAX][kSfxTile + 1];
+    __shared__ float red[4][GMAX];
+    __shared__ float m_s[GMAX], l_s[GMAX], al_s[GMAX];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = Hq / H;
+    const int unit = blockIdx.x;                    // (layer * A + a) * H + h
+    const int h = unit % H;
+    const int la = unit / H;                        // layer * A + a
+    const uint16_t* kbase = sk + (int64_t)unit * S * D;
+    const uint16_t* vbase = sv + (int64_t)unit * S * D;
+
+    for (int i = tid; i < GMAX * D; i += kSfxThreads) {
+        const int g = i / D, j = i % D;
+        qs[g][j] = g < G ? bits_to_float(q[((int64_t)la * Hq + h * G + g) * D + j], BF16) : 0.0f;
+    }
+    if (tid < GMAX) {
+        m_s[tid] = -INFINITY;
+        l_s[tid] = 0.0f;
+    }
+    // accumulator: column j = tid (and tid + 128 / 64 rows split for D = 64 handled by the loop)
+    constexpr int CPT = (D + kSfxThreads - 1) / kSfxThreads;   // columns per thread
+    float acc[GMAX][CPT];
+#pragma unroll
+    for (int g = 0; g < GMAX; ++g)
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) acc[g][c] = 0.0f;
+    __syncthreads();
+
+    for (int64_t t0 = 0; t0 < S; t0 += kSfxTile) {
+        // scores: thread = token
+        const int64_t t = t0 + tid;
+        const bool valid = t < S;
+        float x[GMAX];
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) x[g] = 0.0f;
+        if (valid) {
+            const uint4* krow = reinterpret_cast<const uint4*>(kbase + t * D);
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 w = krow[c];
+                const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float k0 = bits_to_float((uint16_t)(wv[e] & 0xFFFFu), BF16);
+                    const float k1 = bits_to_float((uint16_t)(wv[e] >> 16), BF16);
+                    const int j = 8 * c + 2 * e;
+#pragma unroll
+                    for (int g = 0; g < GMAX; ++g) x[g] = fmaf(qs[g][j + 1], k1, fmaf(qs[g][j], k0, x[g]));
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            x[g] = valid ? x[g] * scale_log2 : -INFINITY;
+            float v = x[g];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) red[warp][g] = v;
+        }
+        __syncthreads();
+        if (tid < GMAX) {
+            const float mt = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
+            const float mo = m_s[tid];
+            const float mn = fmaxf(mo, mt);
+            al_s[tid] = mo == -INFINITY ? 0.0f : exp2f(mo - mn);
+            m_s[tid] = mn;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            const float p = valid ? exp2f(x[g] - m_s[g]) : 0.0f;
+            ps[g][tid] = p;
+            float v = p;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red[warp][g] = v;
+        }
+        __syncthreads();
+        if (tid < GMAX) l_s[tid] = l_s[tid] * al_s[tid] + red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
+        // values: thread = column
+        const int tmax = (int)((S - t0) < kSfxTile ? (S - t0) : kSfxTile);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+            const int j = tid + c * kSfxThreads;
+            if (j < D) {
+#pragma unroll
+                for (int g = 0; g < GMAX; ++g) acc[g][c] *= al_s[g];
+                for (int tt = 0; tt < tmax; ++tt) {
+                    const float vv = bits_to_float(vbase[(t0 + tt) * D + j], BF16);
+#pragma unroll
+                    for (int g = 0; g < GMAX; ++g) acc[g][c] = fmaf(ps[g][tt], vv, acc[g][c]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    // partial per query head hq = h*G + g of agent a
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+        const int j = tid + c * kSfxThreads;
+        if (j < D)
+            for (int g = 0; g < G && g < GMAX; ++g) acc_out[((int64_t)la * Hq + h * G + g) * D + j] = acc[g][c];
+    }
+    if (tid < G) {
+        ml_out[((int64_t)la * Hq + h * G + tid) * 2] = m_s[tid];
+        ml_out[((int64_t)la * Hq + h * G + tid) * 2 + 1] = l_s[tid];
+    }
+}
+
+template <int D, bool BF16>
+polykv_status run_suffix(const SuffixArgs& a, int L, int A, int H, int Hq, float scale, cudaStream_t st) {
+    const int G = Hq / H;
+    const unsigned blocks = (unsigned)((int64_t)L * A * H);
+    const float sl = scale * 1.4426950408889634f;
+    if (G <= 4)
+        suffix_partial<D, 4, BF16><<<blocks, kSfxThreads, 0, st>>>(
+            static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), static_cast<const uint16_t*>(a.v), A,
+            H, Hq, a.len, sl, a.acc, a.ml);
+    else
+        suffix_partial<D, 16, BF16><<<blocks, kSfxThreads, 0, st>>>(
+            static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), static_cast<const uint16_t*>(a.v), A,
+            H, Hq, a.len, sl, a.acc, a.ml);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "suffix launch: %s", cudaGetErrorString(e));
+    return POLYKV_OK;
+}
+
+}  // namespace
+
+polykv_status launch_attend_suffix(const SuffixArgs& a, polykv_dtype dt, int L, int A, int H, int Hq, int D,
+                                   float scale, cudaStream_t st) {
+    const bool bf = dt == POLYKV_BF16;
+    if (D == 128) return bf ? run_suffix<128, true>(a, L, A, H, Hq, scale, st) : run_suffix<128, false>(a, L, A, H, Hq, scale, st);
+    if (D == 64) return bf ? run_suffix<64, true>(a, L, A, H, Hq, scale, st) : run_suffix<64, false>(a, L, A, H, Hq, scale, st);
+    return set_error(POLYKV_E_UNSUPPORTED, "suffix: head_dim %d", D);
+}
+
+}  // namespace polykv

@@ -762,7 +762,7 @@ size_t attend_tc_workspace(const PoolView& p, int rows, int64_t n_ctx) {
 
 polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
                                int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const SuffixArgs* sfx) {
     const int G = n_q_heads / p.H;
     const int R = n_agents * G;
     if (!attend_tc_supported(p, R)) return set_error(POLYKV_E_UNSUPPORTED, "tensor-core attend: d=%d rows=%d", p.d, R);
@@ -795,8 +795,12 @@ polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q
     kern<<<pl.nctas, kThreadsTc, kSmBytes, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_tc launch: %s", cudaGetErrorString(e));
+    if (sfx) {
+        const polykv_status ss = launch_attend_suffix(*sfx, dt, p.L, n_agents, p.H, n_q_heads, kD, scale, stream);
+        if (ss != POLYKV_OK) return ss;
+    }
     return launch_attend_merge(P.ws_acc, P.ws_ml, out, (int)U, p.H, n_agents, n_q_heads, R, pl.pmax, pl.nt, pl.tt,
-                               pl.nctas, kD, stream);
+                               pl.nctas, kD, stream, sfx ? sfx->acc : nullptr, sfx ? sfx->ml : nullptr);
 }
 
 }  // namespace polykv

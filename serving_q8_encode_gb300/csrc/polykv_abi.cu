@@ -271,6 +271,62 @@ polykv_status polykv_pool_status(const polykv_pool* pool, void* stream, uint32_t
     return POLYKV_OK;
 }
 
+static size_t suffix_bytes(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads) {
+    const size_t rows = (size_t)pool->desc.n_layers * (size_t)n_agents * (size_t)n_q_heads;
+    return sizeof(float) * rows * ((size_t)pool->desc.head_dim + 2);
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+polykv_status polykv_attend_ex_workspace_size(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads,
+                                              int64_t n_ctx, const polykv_attend_ext* ext, size_t* bytes) {
+    const polykv_status st = check_attend_args(pool, n_agents, n_q_heads, n_ctx);
+    if (st != POLYKV_OK) return st;
+    if (!bytes) return set_error(POLYKV_E_INVAL, "bytes is NULL");
+    const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
+    size_t b = attend_workspace(pool->view, rows, n_ctx);
+    if (ext && ext->suffix_len > 0) b = align256(b) + suffix_bytes(pool, n_agents, n_q_heads);
+    *bytes = b;
+    return POLYKV_OK;
+}
+
+polykv_status polykv_attend_ex(const polykv_pool* pool, const void* q, float* out, int32_t n_agents,
+                               int32_t n_q_heads, int64_t n_ctx, float softmax_scale, const polykv_attend_ext* ext,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    if (!ext || ext->suffix_len == 0)
+        return polykv_attend(pool, q, out, n_agents, n_q_heads, n_ctx, softmax_scale, workspace, workspace_bytes,
+                             stream);
+    const polykv_status st = check_attend_args(pool, n_agents, n_q_heads, n_ctx);
+    if (st != POLYKV_OK) return st;
+    if (!q || !out || !workspace) return set_error(POLYKV_E_INVAL, "q, out and workspace must be non-NULL");
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace))
+        return set_error(POLYKV_E_INVAL, "q, out and workspace must be 16-byte aligned");
+    if (ext->suffix_len < 0) return set_error(POLYKV_E_INVAL, "suffix_len must be >= 0");
+    if (!ext->suffix_k || !ext->suffix_v || !aligned16(ext->suffix_k) || !aligned16(ext->suffix_v))
+        return set_error(POLYKV_E_INVAL, "suffix_k and suffix_v must be non-NULL and 16-byte aligned");
+    if (n_q_heads / pool->desc.n_kv_heads > 16)
+        return set_error(POLYKV_E_UNSUPPORTED, "suffix: more than 16 query heads per kv head");
+    const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
+    const size_t pool_ws = attend_workspace(pool->view, rows, n_ctx);
+    const size_t need = align256(pool_ws) + suffix_bytes(pool, n_agents, n_q_heads);
+    if (workspace_bytes < need)
+        return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend_ex: workspace %zu < %zu bytes", workspace_bytes, need);
+    const size_t nrows = (size_t)pool->desc.n_layers * (size_t)n_agents * (size_t)n_q_heads;
+    SuffixArgs sfx;
+    sfx.q = q;
+    sfx.k = ext->suffix_k;
+    sfx.v = ext->suffix_v;
+    sfx.len = ext->suffix_len;
+    sfx.acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(pool_ws));
+    sfx.ml = sfx.acc + nrows * (size_t)pool->desc.head_dim;
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
+    if (use_tc_path(pool->view, rows))
+        return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
+                                pool_ws, static_cast<cudaStream_t>(stream), &sfx);
+    return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
+                              pool_ws, static_cast<cudaStream_t>(stream), &sfx);
+}
+
 polykv_status polykv_free(polykv_pool* pool) {
     delete pool;
     return POLYKV_OK;

@@ -41,22 +41,36 @@ polykv_status set_error(polykv_status st, const char* fmt, ...);
 polykv_status launch_encode(const PoolView& p, polykv_dtype dt, const void* k, const void* v, int64_t t0,
                             int64_t n_tokens, cudaStream_t stream);
 
+// Private per-agent suffix (uncompressed keys/values [L][A][H][len][d]) and its partials
+// (acc [L][A][Hq][d] in the original basis, (m, l) [L][A][Hq][2]).
+struct SuffixArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    int64_t len;
+    float* acc;
+    float* ml;
+};
+polykv_status launch_attend_suffix(const SuffixArgs& a, polykv_dtype dt, int L, int A, int H, int Hq, int D,
+                                   float scale, cudaStream_t st);
+
 // number of token splits used by the CUDA-core attention path
 int attend_simt_splits(const PoolView& p, int rows, int64_t n_ctx);
 size_t attend_simt_workspace(const PoolView& p, int rows, int64_t n_ctx);
 polykv_status launch_attend_simt(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
                                  int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const SuffixArgs* sfx = nullptr);
 
 polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float* out, int U, int H, int A, int Hq,
-                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st);
+                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st,
+                                  const float* sfx_acc = nullptr, const float* sfx_ml = nullptr);
 
 // tensor-core attention path (head_dim 128, up to 64 rows per kv head)
 bool attend_tc_supported(const PoolView& p, int rows);
 size_t attend_tc_workspace(const PoolView& p, int rows, int64_t n_ctx);
 polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
                                int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const SuffixArgs* sfx = nullptr);
 
 __host__ __device__ inline float centroid_of(int code) {
     // ascending codes 0..7 -> -c7 .. -c4, c4 .. c7

@@ -212,3 +212,37 @@ def test_tiny_key_blocks_subnormal_scales(env):
     ref = oracle.attention.encode_pool(kb, vb, "bf16", b32)
     assert np.any(np.abs(ref["k_codes"].astype(int)) == 127)
     check_encode(pool, ref, T, 0, b32)
+
+
+# ---- pool + private per-agent suffix under one softmax
+def run_suffix_case(env, L, H, Hq, d, T, A, S, dtype, seed=0, q_mult=1.0):
+    pk, torch, c32, b32 = env
+    kb, vb = synth.gen_kv(L, H, T, d, dtype, seed)
+    qb = synth.gen_q(L, A, Hq, d, dtype, seed, q_mult=q_mult)
+    sk, sv = synth.gen_suffix(L, A, H, S, d, dtype, seed)
+    pool = pk.Pool(L, H, d, T, dtype)
+    pool.encode(_dev(torch, kb), _dev(torch, vb))
+    out = pool.attend_with_suffix(_dev(torch, qb), T, _dev(torch, sk), _dev(torch, sv))
+    torch.cuda.synchronize()
+    assert pool.status() == 0
+    ref_pool = oracle.attention.encode_pool(kb, vb, dtype, b32)
+    ref = oracle.attention.attend_pool(qb, dtype, ref_pool, T, c32, suffix_k_bits=sk, suffix_v_bits=sv)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() <= ATOL, f"max abs err {err.max():.3e}"
+
+
+def test_suffix_llama3_8b_7194_pool_256_private(env, path):
+    run_suffix_case(env, 2, 8, 32, 128, 7194, 15, 256, "bf16")
+
+
+@pytest.mark.parametrize("S", [1, 33, 300])
+def test_suffix_ragged_lengths(env, path, S):
+    run_suffix_case(env, 1, 4, 16, 128, 200, 3, S, "bf16", seed=S)
+
+
+def test_suffix_smollm2_mha_fp16(env, path):
+    run_suffix_case(env, 2, 32, 32, 64, 600, 2, 64, "f16")
+
+
+def test_suffix_peaky(env, path):
+    run_suffix_case(env, 1, 2, 8, 128, 500, 2, 128, "bf16", q_mult=8.0)
