@@ -31,12 +31,13 @@ DEFAULT_WORKLOAD = "llama3_8b_4096_a15"
 
 
 def algorithmic_bytes(w: synth.Workload, n_ctx: int, n_agents: int):
-    """(encode bytes, attend bytes) per call, from the pool format."""
+    """(encode bytes, attend bytes) per call, from the pool format (plus the private suffixes)."""
     L, H, Hq, d = w.n_layers, w.n_kv_heads, w.n_q_heads, w.head_dim
     per_tok_pool = d + 2 * (d // 32) + 3 * d // 8 + 2
     pool = L * H * n_ctx * per_tok_pool
     enc = L * H * n_ctx * d * 2 * 2 + pool          # read K, V (16-bit), write the pool
     att = pool + L * n_agents * Hq * d * 2 + L * n_agents * Hq * d * 4   # pool + q + fp32 out
+    att += L * n_agents * H * w.suffix_len * d * 2 * 2                   # private suffix K, V
     return enc, att
 
 
@@ -209,14 +210,25 @@ def run_polykv(args, w: synth.Workload):
     pool = pk.Pool(L, H, d, T, w.dtype, device=dev)
     out = torch.empty((L, A, Hq, d), dtype=torch.float32, device=dev)
     pool.encode(k, v)  # so the prefix is valid for the workspace query
-    ws = torch.empty(max(16, pool.workspace_size(A, Hq, T)), dtype=torch.uint8, device=dev)
+    ext = None
+    if w.suffix_len:
+        skb, svb = synth.gen_suffix(L, A, H, w.suffix_len, d, w.dtype, seed=rank)
+        sk = torch.from_numpy(skb.view(np.int16)).to(dev)
+        sv = torch.from_numpy(svb.view(np.int16)).to(dev)
+        ext = pk.AttendExt(sk.data_ptr(), sv.data_ptr(), w.suffix_len)
+    ws = torch.empty(max(16, pk.polykv_attend_ex_workspace_size(pool.handle, A, Hq, T, ext)), dtype=torch.uint8,
+                     device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def attend():
+        pk.polykv_attend_ex(pool.handle, q.data_ptr(), out.data_ptr(), A, Hq, T, 0.0, ext, ws.data_ptr(), ws.numel(),
+                            stream.cuda_stream)
+
     def step():
         pool.encode(k, v, stream=stream)
-        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+        attend()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -233,7 +245,7 @@ def run_polykv(args, w: synth.Workload):
         ev[i][0].record(stream)
         pool.encode(k, v, stream=stream)
         ev[i][1].record(stream)
-        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+        attend()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -250,7 +262,7 @@ def run_polykv(args, w: synth.Workload):
         flush.fill_(float(i))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+        attend()
         e1.record(stream)
         e1.synchronize()
         att_alone.append(e0.elapsed_time(e1))
@@ -269,7 +281,7 @@ def run_polykv(args, w: synth.Workload):
         v.copy_(hv, non_blocking=True)
         q.copy_(hq, non_blocking=True)
         pool.encode(k, v, stream=stream)
-        pool.attend(q, T, out=out, workspace=ws, stream=stream)
+        attend()
         hout.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         if i > 0:
@@ -299,10 +311,11 @@ def run_polykv(args, w: synth.Workload):
     if dominant == "encode":
         kname, kbytes, kms, files = "encode_kernel", enc_b, enc_ms_m, ["encode.cu"]
     else:
-        kname, kbytes, kms, files = "attend", att_b, att_ms_m, ["attend_simt.cu"]
+        kname, kbytes, kms, files = "attend", att_b, att_ms_m, ["attend_tc.cu", "attend_simt.cu", "attend_suffix.cu"]
     achieved = kbytes / (kms * 1e-3) / 1e9
     traffic = traffic_from_profiles(kname, w.name, kernel_source_hash(files))
-    att_traffic = traffic_from_profiles("attend", w.name, kernel_source_hash(["attend_simt.cu"]))
+    att_traffic = traffic_from_profiles("attend", w.name,
+                                        kernel_source_hash(["attend_tc.cu", "attend_simt.cu", "attend_suffix.cu"]))
     h2d = kb.nbytes + vb.nbytes + qb.nbytes
     d2h = L * A * Hq * d * 4
     if rank != 0:
@@ -321,7 +334,7 @@ def run_polykv(args, w: synth.Workload):
                      "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": world * (enc_b + att_b) / (e2e_ms_m * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_m},
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps * (3 + (1 if w.suffix_len else 0)),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -329,6 +342,66 @@ def run_polykv(args, w: synth.Workload):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(args):
+    """Encode-only and attend-only throughput at the Llama-3-8B shape over the pages' context lengths
+    and agent counts; one JSON object with the grid (not the driver's single bench line)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import serving_q8_encode_gb300 as pk
+
+    base = synth.WORKLOADS[DEFAULT_WORKLOAD]
+    L, H, Hq, d = base.n_layers, base.n_kv_heads, base.n_q_heads, base.head_dim
+    dev = torch.device("cuda", 0)
+    peak, peak_src = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    rows = []
+    for T in (600, 1851, 4096, 7194):
+        kb, vb = synth.gen_kv(L, H, T, d, base.dtype, seed=0)
+        k = torch.from_numpy(kb.view(np.int16)).to(dev)
+        v = torch.from_numpy(vb.view(np.int16)).to(dev)
+        del kb, vb
+        pool = pk.Pool(L, H, d, T, base.dtype, device=dev)
+        pool.encode(k, v)
+
+        def timed(fn, reps):
+            ts = []
+            for i in range(reps + 2):
+                flush.fill_(float(i))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    ts.append(e0.elapsed_time(e1) * 1e3)
+            return float(np.median(ts))
+
+        w = synth.Workload("sweep", L, H, Hq, d, T, 1, base.dtype)
+        enc_b, _ = algorithmic_bytes(w, T, 1)
+        enc_us = timed(lambda: pool.encode(k, v, stream=stream), args.steps)
+        rows.append({"mode": "encode", "n_ctx": T, "us": enc_us, "tokens_per_s": T / (enc_us * 1e-6),
+                     "gbs": enc_b / (enc_us * 1e-6) / 1e9})
+        for A in (1, 2, 4, 8, 15):
+            qb = synth.gen_q(L, A, Hq, d, base.dtype, seed=0)
+            q = torch.from_numpy(qb.view(np.int16)).to(dev)
+            out = torch.empty((L, A, Hq, d), dtype=torch.float32, device=dev)
+            ws = torch.empty(max(16, pool.workspace_size(A, Hq, T)), dtype=torch.uint8, device=dev)
+            _, att_b = algorithmic_bytes(w, T, A)
+            att_us = timed(lambda: pool.attend(q, T, out=out, workspace=ws, stream=stream), args.steps)
+            rows.append({"mode": "attend", "n_ctx": T, "n_agents": A, "us": att_us,
+                         "gbs": att_b / (att_us * 1e-6) / 1e9, "frac_of_peak": att_b / (att_us * 1e-6) / 1e9 / peak,
+                         "pool_bytes": att_b - L * A * Hq * d * 6})
+        del pool, k, v
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "llama3_8b shape, encode-only and attend-only", "peak_gbs": peak,
+                      "peak_source": peak_src, "l2": "flushed before each launch", "rows": rows}), flush=True)
     return 0
 
 
@@ -341,6 +414,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--sweep", action="store_true",
+                    help="encode-only / attend-only grid over context {600,1851,4096,7194} x agents {1,2,4,8,15}")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (smaller cases for profiler captures)")
     args = ap.parse_args()
@@ -348,6 +423,8 @@ def main():
     if args.layers is not None:
         import dataclasses
         w = dataclasses.replace(w, n_layers=args.layers, name=f"{w.name}_L{args.layers}")
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_polykv(args, w)
