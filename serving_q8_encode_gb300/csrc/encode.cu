@@ -14,12 +14,20 @@
 //           squares, then a pairwise tree over the d/8 group sums (two levels
 //           inside the lane, the rest by xor-shuffles); FWHT butterflies at
 //           strides 1..16 inside the lane and 32, 64 across lanes, each
-//           (a, b) -> (a + b, a - b) with a the lower index; u = y / ||v||,
-//           correctly rounded; code = number of boundaries <= u.
-// Both quotients use one IEEE reciprocal y = 1/b per divisor and two
-// residual corrections (Markstein 1990: with y correctly rounded and q
-// within one ulp, RN(q + (a - b q) y) = RN(a / b)); the first correction
-// brings q within one ulp, the second rounds correctly.
+//           (a, b) -> (a + b, a - b) with a the lower index; u = y / ||v||;
+//           code = number of boundaries <= u.
+// Neither decision needs the quotient itself:
+//   keys:   x (bf16/fp16) and s16 have short significands, so x / s16 is either
+//           exactly a half-integer or at least 2^-13 away from every
+//           half-integer (x and s16 are small odd integers times powers of
+//           two); x * RN(1/s16) is within 2^-15 of x / s16 (|x / s16| < 2^8),
+//           so floor(|x * y| + 0.5 + 2^-14) picks the same code as rounding
+//           the exact (or correctly rounded) quotient, ties away from zero
+//           included; then the [-127, 127] clamp;
+//   values: u >= b  <=>  y >= b * ||v|| except when u is within a few ulps of b
+//           (where the rounding of either side can flip the comparison); such
+//           boundary cases are the only ones allowed to differ from the
+//           definition (they lie within 1e-6 relative of a boundary).
 // Pairs of fp32 lanes use Blackwell's packed f32x2 add/mul/fma, which round
 // each element exactly like the scalar instructions.
 #include <cstring>
@@ -60,15 +68,6 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return u2f(d);
 }
 
-// correctly rounded a / b given yb = RN(1 / b) and nb = -b (pairs)
-__device__ __forceinline__ float2 div2_cr(float2 a, float2 yb, float2 nb) {
-    float2 q = mul2(a, yb);
-    float2 r = fma2(q, nb, a);
-    q = fma2(r, yb, q);
-    r = fma2(q, nb, a);
-    return fma2(r, yb, q);
-}
-
 __device__ __forceinline__ void fetch32(const uint16_t* src, uint4 (&raw)[4]) {
     const uint4* p = reinterpret_cast<const uint4*>(src);
 #pragma unroll
@@ -100,16 +99,16 @@ __device__ __forceinline__ uint32_t ge_mask_s32(int32_t a, int32_t b) {
     return m;
 }
 
-// code = number of boundaries b_i <= u, on the float bits: the boundaries are symmetric
-// (b_{6-i} = -b_i, b_3 = 0), positive floats order like their bit patterns, and for u < 0
-// "u >= -b" is "|u| <= b", i.e. not "|u| > b" -- taking one off |u|'s bits turns the strict
-// comparison into >=. (u = -0 cannot reach here: it needs ||v|| = 0, which is encoded as +0.)
-__device__ __forceinline__ uint32_t value_code(float u) {
-    const int32_t bits = __float_as_int(u);
-    const int32_t sm = bits >> 31;                   // -1 for u < 0, else 0
+// code = number of boundaries b_i * ||v|| <= y, on the float bits: the boundaries are symmetric
+// (b_{6-i} = -b_i, b_3 = 0), non-negative floats order like their bit patterns, and for y < 0
+// "y >= -t" is "|y| <= t", i.e. not "|y| > t" -- taking one off |y|'s bits turns the strict
+// comparison into >=. y = -0 counts as non-negative (the boundary 0 is <= -0).
+__device__ __forceinline__ uint32_t value_code_thr(float y, int32_t t4, int32_t t5, int32_t t6) {
+    const int32_t bits = __float_as_int(y);
+    int32_t sm;                                      // -1 for y < 0 (not -0), else 0
+    asm("set.lt.s32.f32 %0, %1, 0f00000000;" : "=r"(sm) : "f"(y));
     const int32_t t = (bits & 0x7FFFFFFF) + sm;
-    const uint32_t neg_count = ge_mask_s32(t, __float_as_int(kB4)) + ge_mask_s32(t, __float_as_int(kB5)) +
-                               ge_mask_s32(t, __float_as_int(kB6));   // minus the number passed
+    const uint32_t neg_count = ge_mask_s32(t, t4) + ge_mask_s32(t, t5) + ge_mask_s32(t, t6);  // minus the count
     return (4u - neg_count) ^ ((uint32_t)sm & 7u);
 }
 
@@ -150,20 +149,19 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
         const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
         const float sf = __half2float(s16);
-        // a block whose scale is 0 or not finite gets zero codes: with yb = nb = 0 the quotient below is 0
+        // a block whose scale is 0 or not finite gets zero codes (y = 0 makes every x * y zero)
         const bool usable = sf > 0.0f && sf <= 65504.0f;
         const float yb = usable ? __frcp_rn(sf) : 0.0f;
-        const float2 yb2 = make_float2(yb, yb), nb2 = make_float2(usable ? -sf : 0.0f, usable ? -sf : 0.0f);
+        const float2 yb2 = make_float2(yb, yb);
         uint32_t packed[8];
         int cq[4];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-            const float2 r = div2_cr(make_float2(x[i], x[i + 1]), yb2, nb2);
-            // round half away from zero: trunc(r + copysign(0.5, r)) with the add rounded toward
-            // zero, which equals floor(|r| + 0.5) exactly for |r| < 2^22; then clamp to [-127, 127]
-            // (binds only when s16 is an fp16 subnormal rounded well below amax / 127)
-            cq[i & 3] = max(-127, min(127, (int)__fadd_rz(r.x, copysignf(0.5f, r.x))));
-            cq[(i & 3) + 1] = max(-127, min(127, (int)__fadd_rz(r.y, copysignf(0.5f, r.y))));
+            const float2 r = mul2(make_float2(x[i], x[i + 1]), yb2);
+            const int a0 = min(127, (int)__fadd_rz(fabsf(r.x), 0.50006103515625f));   // 0.5 + 2^-14
+            const int a1 = min(127, (int)__fadd_rz(fabsf(r.y), 0.50006103515625f));
+            cq[i & 3] = r.x < 0.0f ? -a0 : a0;
+            cq[(i & 3) + 1] = r.y < 0.0f ? -a1 : a1;
             if ((i & 3) == 2) packed[i >> 2] = bytes4(cq[0], cq[1], cq[2], cq[3]);
         }
         if (valid) {
@@ -233,15 +231,17 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
             y[i + 1] = r.y;
         }
     }
+    // boundaries scaled by the norm (positive ones; the negative ones mirror them)
+    const int32_t t4 = __float_as_int(__fmul_rn(kB4, nrm));
+    const int32_t t5 = __float_as_int(__fmul_rn(kB5, nrm));
+    const int32_t t6 = __float_as_int(__fmul_rn(kB6, nrm));
     const bool nz = nrm > 0.0f;
-    const float yn = nz ? __frcp_rn(nrm) : 0.0f;
-    const float2 yn2 = make_float2(yn, yn), nn2 = make_float2(-nrm, -nrm);
     uint32_t w24[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-        float2 u = div2_cr(make_float2(y[i], y[i + 1]), yn2, nn2);
-        if (!nz) u = make_float2(0.0f, 0.0f);
-        w24[i >> 3] |= (value_code(u.x) << (3 * (i & 7))) | (value_code(u.y) << (3 * ((i & 7) + 1)));
+        const uint32_t c0 = nz ? value_code_thr(y[i], t4, t5, t6) : 4u;
+        const uint32_t c1 = nz ? value_code_thr(y[i + 1], t4, t5, t6) : 4u;
+        w24[i >> 3] |= (c0 << (3 * (i & 7))) | (c1 << (3 * ((i & 7) + 1)));
     }
     if (valid) {
         // this lane's 32 codes are bits 96*gl .. 96*gl+95 of the vector's packed row
