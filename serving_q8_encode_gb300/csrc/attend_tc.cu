@@ -7,35 +7,41 @@
 // agents x 4 GQA heads = 60 rows per kv head, q.K and p.V are dense
 // contractions (about 156 flop per pool byte), so both run as tcgen05.mma:
 //
-//   MMA1 (per 128-token tile, per 32-wide q8_0 block b):
-//        S_b^T[token][row] = K_b[token][32] . Q_b[row][32]^T
-//        A = int8 key codes converted exactly to fp16 and written to TMEM by
-//        the producer warps; B = the rows' queries in fp16, scaled by a power of
-//        two (bf16 queries are then represented exactly); four fp32
-//        accumulators so each block's fp16 scale multiplies its own partial
-//        sum, as in the q8_0 definition.
+//   MMA1 (per 128-token tile): S^T[token][row] = K_hat[token][128] . Q'[row][128]^T
+//        with K_hat = s_b * code * 2^-4 split exactly into two fp16 halves
+//        (hi = fp16(K_hat), lo = K_hat - hi; the product has at most 18
+//        significant bits, so hi + lo = K_hat) held in TMEM as the A operand,
+//        and Q' the rows' queries in fp16 scaled by a power of two (bf16
+//        queries are then exact). One fp32 accumulator sums hi then lo.
 //   softmax (one thread per token and row group; TMEM lane = token):
-//        x = sum_b s_b * S_b (base-2 logits), online max with lazy rescaling
-//        (only when a logit exceeds the running max by more than 2^6),
-//        p = 2^(x - m), P' = p * ||v|| * w in fp16, w a power of two from the
-//        pool's per-unit norm maximum (so P' < 2^14).
-//   MMA2: O^T[dim][row] += Vc[token][dim]^T . P'[token][row], A = the 3-bit
-//        value codes expanded to fp16 centroids in the ROTATED basis; the
-//        inverse FWHT is applied once per output row by the merge kernel.
+//        d = c * S - m (base-2 logits relative to the running max), lazy
+//        rescaling only when some d exceeds 2^8 (decided for the whole row
+//        group with one OR-reducing barrier), p = 2^d stored as fp16.
+//   MMA2: O^T[dim][row] += Vn[token][dim]^T . P[token][row], where
+//        Vn = centroid(code) * ||v|| * w in fp16 (w a power of two from the
+//        pool's per-unit norm maximum, so ||v|| w < 2^8): the value operand
+//        carries its norm, in the ROTATED basis; the merge kernel applies the
+//        inverse FWHT once per output row.
 //
-// Data movement: one TMA thread streams each 128-token tile of the pool
-// (key codes as a 128B-swizzled 2-D tile, scales / value codes / norms as
-// 1-D bulk copies) into a 4-deep shared-memory ring, so about 95 KB per SM
-// are in flight; every pool byte is read from HBM once for all agents.
-// Work: the (layer, kv head, tile) list is cut into one contiguous range per
-// CTA (one persistent CTA per SM); a range that crosses a unit boundary
-// writes one softmax partial per unit piece; the merge kernel combines them.
+// Data movement: one TMA thread streams each tile's block scales, value codes
+// and norms (7.25 KB) into a 4-deep shared-memory ring; the key-code rows
+// (16 KB per tile) are copied by the producer warps themselves with cp.async,
+// one own tile ahead, into padded per-token rows. The ring's readers fence
+// the async proxy before releasing a stage (the TMA refill is an async-proxy
+// write after their generic loads). Every pool byte is read from HBM
+// once for all agents. The (layer, kv head, tile) list is cut into one
+// contiguous range per CTA (one persistent CTA per SM); a range that crosses a
+// unit boundary writes one softmax partial per unit piece; the merge kernel
+// combines them.
 //
-// Warp roles (448 threads): 0-3 producers (key codes -> TMEM, value codes ->
-// centroids in shared memory), 4-11 softmax in two row groups of 32, 12 MMA
-// issue + TMEM owner, 13 TMA. Every mbarrier wait is bounded (2 s); on expiry
-// the CTA raises an abort flag, skips the rest of its work, waits (bounded)
-// for its copies in flight, frees its TMEM and sets the pool's status word.
+// Warp roles (576 threads): 0-7 producers in two groups of four warps that
+// take alternate tiles (each thread: one token's key codes -> exact hi/lo fp16
+// in TMEM, then its value codes -> norm-scaled centroids in shared memory),
+// 8-15 softmax in two row groups of 32, 16 MMA issue (an event loop over both
+// MMA chains) + TMEM owner, 17 TMA. Every mbarrier wait is bounded
+// (2 s); on expiry the CTA raises an abort flag, skips the rest of its work,
+// waits (bounded) for its copies in flight, frees its TMEM and sets the pool's
+// status word.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -49,26 +55,31 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kNR = 64;            // padded rows (MMA N)
-constexpr int kThreadsTc = 448;
-constexpr int kNS = 8;             // pool-tile ring depth
-constexpr float kTau = 6.0f;       // lazy rescale threshold (log2 units)
+constexpr int kThreadsTc = 576;    // 18 warps
+constexpr int kNS = 4;             // ring depth: scales / value codes / norms
+constexpr int kKS = 4;             // key-row stages: two per producer group (cp.async, one own tile ahead)
+constexpr float kTau = 8.0f;       // lazy rescale threshold (log2 units): p <= 2^8
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kLog2eTc = 1.4426950408889634f;
 
-// one ring stage: block scales | value codes | norms (the key codes go straight to registers)
+// one ring stage: block scales | value codes | norms
 constexpr uint32_t kRawS = 0, kRawV = 1024, kRawN = 7168;
 constexpr uint32_t kRawBytes = 7424;       // bytes delivered per tile
 constexpr uint32_t kRawStage = 7424;
+constexpr uint32_t kKRow = 144;            // padded key row: 8-lane phases of 16-byte loads hit distinct banks
+constexpr uint32_t kKStage = kTile * kKRow;
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kSmQ = 0;                            // 2 chunks x [64 rows][128 B]          16 KB
-constexpr uint32_t kSmV = kSmQ + 16384;                 // 2 stages x 2 dim blocks x [128][128 B] 64 KB
-constexpr uint32_t kSmP = kSmV + 65536;                 // 2 stages x [128 tokens][128 B]       32 KB
-constexpr uint32_t kSmRaw = kSmP + 32768;               // kNS x 7.25 KB                        58 KB
-constexpr uint32_t kSmLut = kSmRaw + kNS * kRawStage;   // 64 code pairs x 32 lanes x 4 B         8 KB
+constexpr uint32_t kSmQ = 0;                            // 2 chunks x [64 rows][128 B]             16 KB
+constexpr uint32_t kSmV = kSmQ + 16384;                 // 2 stages x 2 dim blocks x [128][128 B]  64 KB
+constexpr uint32_t kSmP = kSmV + 65536;                 // 2 stages x [128 tokens][128 B]          32 KB
+constexpr uint32_t kSmRaw = kSmP + 32768;               // kNS x 7.25 KB                           29 KB
+constexpr uint32_t kSmK = kSmRaw + kNS * kRawStage;     // kKS x 128 x 144 B                       72 KB
+constexpr uint32_t kSmLut = kSmK + kKS * kKStage;       // 64 code pairs x 32 lanes x 4 B            8 KB
 constexpr uint32_t kSmMisc = kSmLut + 8192;
-constexpr uint32_t kSmBytes = kSmMisc + 2048 + 1024;    // + alignment slack
+constexpr uint32_t kSmBytes = kSmMisc + 3072 + 1024;    // + alignment slack
 static_assert(kSmBytes <= 232448, "shared memory budget");
+static_assert(kSmK % 16 == 0 && kKRow % 16 == 0, "cp.async destinations are 16-byte aligned");
 
 // TMEM columns
 constexpr uint32_t kColK = 0;     // 2 stages x (64 hi + 64 lo)
@@ -93,20 +104,20 @@ struct TcParams {
 };
 
 struct Misc {
-    float msm[kNR];       // running max per row (log2 units)
-    float alpha[kNR];
+    float m[kNR];         // running max per row (log2 units); +inf for padding rows
+    float nm[kNR];        // -m
+    float alpha[kNR];     // 2^(m_old - m_new)
     float red[2][4][32];
     float qred[8];
     float scale_eff;
     float wscale;
-    int flags[2][3];
     int abort;
     int pad;
     uint64_t kfull[2], kfree[2], vfull[2], pfull[2], pvfree[2], sfull[2], sfree[2], qready, done;
     uint64_t rfull[kNS], rempty[kNS];
     uint32_t tslot;
 };
-static_assert(sizeof(Misc) <= 2048, "misc block");
+static_assert(sizeof(Misc) <= 3072, "misc block");
 
 __device__ __forceinline__ int64_t cta_of_tile(int64_t g, int64_t tt, int nc) { return ((g + 1) * nc - 1) / tt; }
 
@@ -131,11 +142,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
     return u2f(d);
 }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
-    return u2f(d);
-}
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
@@ -145,6 +151,35 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
     return u2f(d);
+}
+
+// OR of `pred` over the `n` threads of named barrier `id`, which all wait here.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.or.pred q, %2, %3, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// 16-byte shared store as inline asm: it stays ahead of the proxy fence and the mbarrier arrive
+// that publish it to the tensor cores (a plain store through a restrict pointer could be moved
+// past them).
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// 16-byte global -> shared copy, zero-filled when src_bytes == 0
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // int8 x4 -> two fp16x2 words, exactly: fp16(0x6400 | (x ^ 0x80)) = 1024 + x + 128.
@@ -172,65 +207,204 @@ __device__ __forceinline__ uint32_t code_pair(const uint32_t (&w)[12]) {
     }
 }
 
-// Four 16-byte chunks (dims 8C..8C+31) of one token's fp16 centroid row: all sixteen
-// code-pair lookups are issued before the four stores, so their latencies overlap.
+// Four 16-byte chunks (dims 8C..8C+31) of one token's value row: centroid pairs looked up
+// (all sixteen issued before the stores) and scaled by the token's ||v|| * w.
 template <int C>
-__device__ __forceinline__ void store_v_quad(const uint32_t (&w)[12], const uint32_t* __restrict__ lut,
-                                             uint8_t* __restrict__ vstage, uint32_t tok, bool valid) {
+__device__ __forceinline__ void store_v_quad(const uint32_t (&w)[12], const uint32_t* lut, uint32_t vstage,
+                                             uint32_t tok, __half2 nw2) {
     uint32_t o[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] = 0u;
-    if (valid) {
 #define PKV_LUT(I) o[I] = lut[code_pair<4 * C + I>(w) * 32];
-        PKV_LUT(0) PKV_LUT(1) PKV_LUT(2) PKV_LUT(3) PKV_LUT(4) PKV_LUT(5) PKV_LUT(6) PKV_LUT(7)
-        PKV_LUT(8) PKV_LUT(9) PKV_LUT(10) PKV_LUT(11) PKV_LUT(12) PKV_LUT(13) PKV_LUT(14) PKV_LUT(15)
+    PKV_LUT(0) PKV_LUT(1) PKV_LUT(2) PKV_LUT(3) PKV_LUT(4) PKV_LUT(5) PKV_LUT(6) PKV_LUT(7)
+    PKV_LUT(8) PKV_LUT(9) PKV_LUT(10) PKV_LUT(11) PKV_LUT(12) PKV_LUT(13) PKV_LUT(14) PKV_LUT(15)
 #undef PKV_LUT
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&o[i]), nw2);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(vstage + ((C + q) / 8) * 16384 + tc::sw128(tok, ((C + q) % 8) * 16)) =
-            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        st_shared16(vstage + ((C + q) / 8) * 16384 + tc::sw128(tok, ((C + q) % 8) * 16), o[4 * q], o[4 * q + 1],
+                    o[4 * q + 2], o[4 * q + 3]);
 }
 
-// Lazy-rescale path of the softmax (rare): with the tile's per-warp row maxima in
-// M.red, the new running max per row of this group, alpha = 2^(m_old - m_new), and
-// O and the per-slot row sums scaled by alpha once MMA2 of the previous tile is done.
-__device__ __noinline__ void softmax_rescale(Misc& M, int grp, int wq, int tt, int rbase, uint32_t gbar, bool first,
-                                             int64_t j, uint32_t lane_addr, volatile int* abortp) {
-                tc::named_bar(gbar, 128);
-                if (tt < 32) {
-                    const int r = rbase + tt;
-                    const float mo = M.msm[r];
-                    const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
-                                           fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
-                    const float mn = fmaxf(mo, mt);
-                    M.alpha[r] = mo == -INFINITY ? 0.0f : (mo == mn ? 1.0f : ex2(mo - mn));
-                    M.msm[r] = mn;
-                }
-                tc::named_bar(gbar, 128);
-                if (!first) {
-                    // O must be scaled before MMA2 of this tile adds to it
-                    tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp,
-                                  kTimeoutNs);
-                    tc::fence_after();
+// Row maxima (in M.red, relative to the running max for a rescale, absolute on a segment's
+// first tile) -> new running max and alpha per row of this group. With `scale_o`, O and
+// the per-slot row sums are scaled by alpha once MMA2 of the previous tile is done.
+__device__ __noinline__ void softmax_new_max(Misc& M, int grp, int tt, int rbase, int R, uint32_t gbar,
+                                             bool seg_first, int64_t j, uint32_t lane_addr, volatile int* abortp) {
+    tc::named_bar(gbar, 128);
+    if (tt < 32) {
+        const int r = rbase + tt;
+        const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
+                               fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
+        if (seg_first) {
+            const float mn = r < R ? mt : INFINITY;
+            M.m[r] = mn;
+            M.nm[r] = -mn;
+            M.alpha[r] = 1.0f;
+        } else if (r < R && mt > 0.0f) {
+            const float mn = M.m[r] + mt;
+            M.alpha[r] = ex2(M.m[r] - mn);
+            M.m[r] = mn;
+            M.nm[r] = -mn;
+        } else {
+            M.alpha[r] = 1.0f;
+        }
+    }
+    tc::named_bar(gbar, 128);
+    if (!seg_first) {
+        // O must be scaled before MMA2 of this tile adds to it
+        tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp, kTimeoutNs);
+        tc::fence_after();
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t to[16], tl[16];
-                        tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
-                        tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
-                        tc::wait_ld();
+        for (int cc = 0; cc < 2; ++cc) {
+            uint32_t to[16], tl[16];
+            tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
+            tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
+            tc::wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float a = M.alpha[rbase + 16 * cc + k];
-                            to[k] = __float_as_uint(__uint_as_float(to[k]) * a);
-                            tl[k] = __float_as_uint(__uint_as_float(tl[k]) * a);
-                        }
-                        tc::tmem_st16(lane_addr + kColO + rbase + 16u * cc, to);
-                        tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
-                    }
-                    tc::wait_st();
-                }
+            for (int k = 0; k < 16; ++k) {
+                const float a = M.alpha[rbase + 16 * cc + k];
+                to[k] = __float_as_uint(__uint_as_float(to[k]) * a);
+                tl[k] = __float_as_uint(__uint_as_float(tl[k]) * a);
             }
+            tc::tmem_st16(lane_addr + kColO + rbase + 16u * cc, to);
+            tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
+        }
+        tc::wait_st();
+    }
+}
+
+// per-segment value scale w = 2^(8 - e), nmax = f * 2^e with f in [0.5, 1): ||v|| * w < 2^8
+__device__ __forceinline__ float unit_wscale(float nmax) {
+    int en = 0;
+    if (nmax > 0.0f) frexpf(nmax, &en);
+    return nmax > 0.0f ? ldexpf(1.0f, 8 - en) : 1.0f;
+}
+
+// Segment prologue (both row groups, 256 threads): the unit's queries in fp16 scaled by a power
+// of two into the MMA1 operand, the logit scale and the value scale w.
+template <bool QBF16>
+__device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, const float* __restrict__ nmax, int64_t u,
+                                              int H, int A, int Hq, int G, int R, float scale_log2, uint8_t* sQ,
+                                              Misc& M, int si, int wi, int lane) {
+    const int layer = (int)(u / H), kvh = (int)(u % H);
+    uint4 qv[4];
+    float qm = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int cid = si + 256 * m;
+        qv[m] = make_uint4(0u, 0u, 0u, 0u);
+        if (cid < R * 16) {
+            const int r = cid >> 4, dc = cid & 15;
+            const int a = r / G, gq = r % G;
+            qv[m] = __ldg(reinterpret_cast<const uint4*>(
+                              q + (((int64_t)layer * A + a) * Hq + kvh * G + gq) * kD) + dc);
+            const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float lo, hi;
+                if (QBF16) {
+                    lo = __uint_as_float(wv[e] << 16);
+                    hi = __uint_as_float(wv[e] & 0xFFFF0000u);
+                } else {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+                    lo = f.x;
+                    hi = f.y;
+                }
+                qm = fmaxf(qm, fmaxf(fabsf(lo), fabsf(hi)));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+    if (lane == 0) M.qred[wi] = qm;
+    tc::named_bar(3, 256);
+    float qmax = 0.0f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) qmax = fmaxf(qmax, M.qred[w8]);
+    int eq = 0;
+    if (qmax > 0.0f) frexpf(qmax, &eq);
+    const float fq = qmax > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;  // qmax * fq in [2^14, 2^15)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int cid = si + 256 * m;
+        if (cid < kNR * 16) {
+            const int r = cid >> 4, dc = cid & 15;
+            const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+            uint32_t hv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float lo = 0.0f, hi = 0.0f;
+                if (r < R) {
+                    if (QBF16) {
+                        lo = __uint_as_float(wv[e] << 16);
+                        hi = __uint_as_float(wv[e] & 0xFFFF0000u);
+                    } else {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+                        lo = f.x;
+                        hi = f.y;
+                    }
+                }
+                const __half2 h = __floats2half2_rn(lo * fq, hi * fq);
+                hv[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            st_shared16(tc::smem_u32(sQ) + (dc >> 3) * 8192 + tc::sw128(r, (dc & 7) * 16), hv[0], hv[1], hv[2], hv[3]);
+        }
+    }
+    if (si == 0) {
+        M.scale_eff = scale_log2 * 16.0f / fq;  // keys are stored in TMEM as s * code * 2^-4
+        M.wscale = unit_wscale(nmax[u]);
+    }
+    tc::fence_proxy_async();
+    tc::named_bar(3, 256);
+    if (si == 0) tc::mbar_arrive(tc::smem_u32(&M.qready));
+}
+
+// Segment epilogue (one row group): row sums over the token slots, then the rows' O^T columns
+// (divided by w) and (m, l) written as the partial for (unit, piece) `slot`.
+__device__ __noinline__ void softmax_epilogue(Misc& M, int s, uint32_t ph, volatile int* abortp, uint32_t lane_addr,
+                                              int grp, int wq, int lane, int tt, int rbase, int R, uint32_t gbar,
+                                              int64_t slot, float* __restrict__ ws_acc, float* __restrict__ ws_ml) {
+    tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph, abortp, kTimeoutNs);
+    tc::fence_after();
+    tc::wait_st();
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        uint32_t tl[16];
+        tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
+        tc::wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            float v = __uint_as_float(tl[k]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 16 * cc + k) M.red[grp][wq][16 * cc + k] = v;
+        }
+    }
+    tc::named_bar(gbar, 128);
+    const float unscale = 1.0f / M.wscale;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        uint32_t to[16];
+        tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
+        tc::wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int r = rbase + 16 * cc + k;
+            if (r < R) ws_acc[(slot * R + r) * kD + tt] = __uint_as_float(to[k]) * unscale;
+        }
+    }
+    if (tt < 32 && rbase + tt < R) {
+        const int r = rbase + tt;
+        ws_ml[(slot * R + r) * 2] = M.m[r];
+        ws_ml[(slot * R + r) * 2 + 1] =
+            M.red[grp][0][tt] + M.red[grp][1][tt] + M.red[grp][2][tt] + M.red[grp][3][tt];
+    }
+    tc::fence_before();
+    tc::named_bar(3, 256);
+}
 
 template <bool QBF16>
 __global__ void __launch_bounds__(kThreadsTc, 1)
@@ -242,6 +416,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint8_t* sV = sm + kSmV;
     uint8_t* sP = sm + kSmP;
     uint8_t* sR = sm + kSmRaw;
+    uint8_t* sK = sm + kSmK;
     uint32_t* lut = reinterpret_cast<uint32_t*>(sm + kSmLut);
     Misc& M = *reinterpret_cast<Misc*>(sm + kSmMisc);
     volatile int* abortp = &M.abort;
@@ -251,7 +426,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int c = blockIdx.x;
     const int64_t g0 = (int64_t)c * TT / P.nctas;
     const int64_t g1 = (int64_t)(c + 1) * TT / P.nctas;
-    const int64_t n = g1 - g0;
+    const int n = (int)(g1 - g0);
     const int nt = P.nt;
     const int64_t cap = P.p.cap;
 
@@ -263,19 +438,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::mbar_init(tc::smem_u32(&M.vfull[s]), 128);
             tc::mbar_init(tc::smem_u32(&M.pfull[s]), 256);
             tc::mbar_init(tc::smem_u32(&M.pvfree[s]), 1);
+            tc::mbar_init(tc::smem_u32(&M.sfull[s]), 1);
+            tc::mbar_init(tc::smem_u32(&M.sfree[s]), 256);
         }
         for (int s = 0; s < kNS; ++s) {
             tc::mbar_init(tc::smem_u32(&M.rfull[s]), 1);
-            tc::mbar_init(tc::smem_u32(&M.rempty[s]), 128 + 256);
-        }
-        for (int s2 = 0; s2 < 2; ++s2) {
-            tc::mbar_init(tc::smem_u32(&M.sfull[s2]), 1);
-            tc::mbar_init(tc::smem_u32(&M.sfree[s2]), 256);
+            tc::mbar_init(tc::smem_u32(&M.rempty[s]), 128);
         }
         tc::mbar_init(tc::smem_u32(&M.qready), 1);
         tc::mbar_init(tc::smem_u32(&M.done), 1);
         M.abort = 0;
-        for (int g = 0; g < 2; ++g) M.flags[g][0] = M.flags[g][1] = M.flags[g][2] = 0;
         tc::mbar_init_fence();
     }
     for (int e = tid; e < 64 * 32; e += kThreadsTc) {
@@ -284,19 +456,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const __half hi = __float2half_rn(centroid_of(idx >> 3));
         lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
     }
-    if (warp == 12) tc::tmem_alloc(tc::smem_u32(&M.tslot), kTmemCols);
+    if (warp == 16) tc::tmem_alloc(tc::smem_u32(&M.tslot), kTmemCols);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tbase = M.tslot;
 
-    if (warp == 13) {
-        // =============================== TMA: pool tiles into the ring
+    if (warp == 17) {
+        // =============================== TMA: scales / value codes / norms into the ring
         if (lane == 0) {
             int issued = 0;
             int64_t u = g0 / nt;
             int ti = (int)(g0 - u * nt);
-            for (int j = 0; j < (int)n && !*abortp; ++j) {
+            for (int j = 0; j < n && !*abortp; ++j) {
                 const int st = j & (kNS - 1);
                 if (j >= kNS &&
                     !tc::mbar_wait(tc::smem_u32(&M.rempty[st]), (uint32_t)(((j / kNS) - 1) & 1), abortp, kTimeoutNs))
@@ -320,38 +492,75 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 tc::mbar_wait(tc::smem_u32(&M.rfull[j & (kNS - 1)]), (uint32_t)((j / kNS) & 1), &dummy, 50000000ull);
             }
         }
-    } else if (warp < 4) {
-        // =============================== producers
-        const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
-        const uint32_t t = (uint32_t)tid;
-        // key rows are read straight from HBM into registers one tile ahead (8 x 16 B per token)
-        int64_t u_n = g0 / nt;
-        int ti_n = (int)(g0 - u_n * nt);
-        uint4 kn[8];
-        auto fetch_k = [&](int64_t uu, int tti) {
-            const int64_t tok = (int64_t)tti * kTile + t;
-            const uint4* src = reinterpret_cast<const uint4*>(P.p.kq + (uu * cap + tok) * kD);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) kn[i] = tok < P.n_ctx ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
-        };
-        if (n > 0) fetch_k(u_n, ti_n);
-        for (int j = 0; j < (int)n && !*abortp; ++j) {
-            const int ti = ti_n;
-            if (++ti_n == nt) {
-                ti_n = 0;
-                ++u_n;
+    } else if (warp < 8) {
+        // =============================== producers: two groups of four warps take alternate tiles
+        // (group pg: tiles pg, pg + 2, ...; TMEM/shared stage pg). Each thread owns one token slot
+        // (= TMEM lane) and writes that token's exact key halves to TMEM, then its norm-scaled value
+        // centroids to shared memory.
+        const int pg = warp >> 2;
+        const uint32_t q4 = (uint32_t)(warp & 3);
+        const uint32_t lane_addr = tbase + ((q4 * 32u) << 16);
+        const uint32_t t = q4 * 32u + (uint32_t)lane;
+        const uint32_t krow = tc::smem_u32(sK) + t * kKRow + (uint32_t)(2 * pg) * kKStage;
+        auto adv2 = [&](int64_t& uu, int& tix) {
+            tix += 2;
+            while (tix >= nt) {
+                tix -= nt;
+                ++uu;
             }
-            const int s = j & 1;
+        };
+        int64_t u_n = (g0 + pg) / nt;
+        int ti_n = (int)((g0 + pg) - u_n * nt);
+        int kk = 0;
+        // copy the key row of this token slot for this group's tile jj into the group's stage kk & 1
+        auto issue_k = [&](int jj) {
+            if (jj < n) {
+                const int64_t tok = (int64_t)ti_n * kTile + t;
+                const bool ok = tok < P.n_ctx;
+                const int8_t* src = P.p.kq + (u_n * cap + (ok ? tok : 0)) * kD;
+                const uint32_t dst = krow + (uint32_t)(kk & 1) * kKStage;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cp_async16(dst + 16u * i, src + 16 * i, ok ? 16u : 0u);
+                adv2(u_n, ti_n);
+            }
+            ++kk;
+            cp_async_commit();
+        };
+        issue_k(pg);
+        int64_t u = (g0 + pg) / nt;
+        int ti = (int)((g0 + pg) - u * nt);
+        float wscale = pg < n ? unit_wscale(P.p.nmax[u]) : 1.0f;
+        const int s = pg;
+        int k = 0;
+        // The loop always runs to its end so that all 128 threads of the group meet at the same
+        // named barriers; after an abort every wait returns at once and the data are ignored.
+        for (int j = pg; j < n; j += 2, ++k) {
             const uint32_t ph = (uint32_t)((j >> 1) & 1);
             const int st = j & (kNS - 1);
             const bool valid = (int64_t)ti * kTile + t < P.n_ctx;
+            issue_k(j + 2);
+            tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs);
+            const uint8_t* raw = sR + st * kRawStage;
+            const uint2 sraw = valid ? *reinterpret_cast<const uint2*>(raw + kRawS + t * 8) : make_uint2(0u, 0u);
+            uint32_t w[12];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const uint4 x = *reinterpret_cast<const uint4*>(raw + kRawV + t * 48 + 16 * i);
+                w[4 * i] = x.x;
+                w[4 * i + 1] = x.y;
+                w[4 * i + 2] = x.z;
+                w[4 * i + 3] = x.w;
+            }
+            const unsigned short nb = *reinterpret_cast<const unsigned short*>(raw + kRawN + t * 2);
+            // the ring stage is refilled by the TMA (async proxy): order these reads before that write
+            tc::fence_proxy_async();
+            tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
+            cp_async_wait<1>();   // this tile's key row has landed (the next one may be in flight)
+            const uint8_t* kr_s = sK + (2 * pg + (k & 1)) * kKStage + t * kKRow;
             // keys: k_hat = s_b * code (times 2^-4 against fp16 overflow) as an exact fp16 pair
             // hi = fp16(k_hat), lo = fp16(k_hat - hi): the product has <= 18 significant bits, hi + lo
             // holds 22, so hi + lo = k_hat and MMA1 over hi then lo gives the exact q . k_hat sums.
-            if (!tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs)) break;
-            const uint8_t* raw = sR + st * kRawStage;
-            const uint2 sraw = valid ? *reinterpret_cast<const uint2*>(raw + kRawS + t * 8) : make_uint2(0u, 0u);
-            if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.kfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
+            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.kfree[s]), ph ^ 1u, abortp, kTimeoutNs);
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {   // q8_0 block qq = dims 32qq .. 32qq+31
                 const uint32_t sw = (qq < 2 ? sraw.x : sraw.y) >> (16 * (qq & 1));
@@ -360,12 +569,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 uint32_t rh[16], rl[16];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint4 kr = kn[2 * qq + h];
+                    const uint4 kr = *reinterpret_cast<const uint4*>(kr_s + 32 * qq + 16 * h);
                     const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint32_t c01, c23;
-                        i8x4_to_f16x4(valid ? kw[e] : 0u, c01, c23);
+                        i8x4_to_f16x4(kw[e], c01, c23);
                         const __half2 h01 = __hmul2(*reinterpret_cast<const __half2*>(&c01), sc);
                         const __half2 h23 = __hmul2(*reinterpret_cast<const __half2*>(&c23), sc);
                         const __half2 l01 = __hfma2(*reinterpret_cast<const __half2*>(&c01), sc, __hneg2(h01));
@@ -382,32 +591,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::wait_st();
             tc::fence_before();
             tc::mbar_arrive(tc::smem_u32(&M.kfull[s]));
-            if (j + 1 < (int)n) fetch_k(u_n, ti_n);  // next tile's key rows, in flight during the value work
-            // values: packed 3-bit codes -> fp16 centroids, token-major rows (MN-major A operand)
-            if (j >= 2 && !tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs)) break;
-            uint32_t w[12];
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                const uint4 x = *reinterpret_cast<const uint4*>(raw + kRawV + t * 48 + 16 * i);
-                w[4 * i] = x.x;
-                w[4 * i + 1] = x.y;
-                w[4 * i + 2] = x.z;
-                w[4 * i + 3] = x.w;
-            }
-            tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
-            store_v_quad<0>(w, lut + lane, sV + s * 32768, t, valid);
-            store_v_quad<4>(w, lut + lane, sV + s * 32768, t, valid);
-            store_v_quad<8>(w, lut + lane, sV + s * 32768, t, valid);
-            store_v_quad<12>(w, lut + lane, sV + s * 32768, t, valid);
+            // values: packed 3-bit codes -> centroids * ||v|| * w in fp16, token-major rows
+            const float nw = valid ? __half2float(__ushort_as_half(nb)) * wscale : 0.0f;
+            const __half2 nw2 = __float2half2_rn(nw);
+            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
+            const uint32_t vst = tc::smem_u32(sV) + s * 32768;
+            store_v_quad<0>(w, lut + lane, vst, t, nw2);
+            store_v_quad<4>(w, lut + lane, vst, t, nw2);
+            store_v_quad<8>(w, lut + lane, vst, t, nw2);
+            store_v_quad<12>(w, lut + lane, vst, t, nw2);
             tc::fence_proxy_async();
             tc::mbar_arrive(tc::smem_u32(&M.vfull[s]));
+            const int64_t u_prev = u;
+            adv2(u, ti);
+            if (u != u_prev && j + 2 < n) wscale = unit_wscale(P.p.nmax[u]);
         }
-    } else if (warp < 12) {
+        cp_async_wait<0>();   // no copy may land in shared memory after the CTA exits
+    } else if (warp < 16) {
         // =============================== softmax + epilogue (two groups of 32 rows)
-        const int grp = (warp - 4) >> 2;        // row group: rows 32*grp .. 32*grp+31
+        const int grp = (warp - 8) >> 2;        // row group: rows 32*grp .. 32*grp+31
         const int wq = warp & 3;                // TMEM lane quadrant
         const int tt = wq * 32 + lane;          // token slot = TMEM lane (= head-dim index in the epilogue)
-        const int si = tid - 128;               // 0..255 over both groups
+        const int si = tid - 256;               // 0..255 over both groups
         const uint32_t lane_addr = tbase + ((uint32_t)(wq * 32) << 16);
         const uint32_t gbar = 1 + grp;
         const int R = P.R;
@@ -416,289 +621,181 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         int64_t seg_u = -1;
         int64_t u = g0 / nt;
         int ti = (int)(g0 - u * nt) - 1;
-        int f3 = 0;  // j mod 3
-        for (int j = 0; j < (int)n; ++j, f3 = (f3 == 2 ? 0 : f3 + 1)) {
+        for (int j = 0; j < n; ++j) {
             if (++ti == nt) {
                 ti = 0;
                 ++u;
             }
             const int s = j & 1;
             const uint32_t ph = (uint32_t)((j >> 1) & 1);
-            const int st = j & (kNS - 1);
             const bool first = (j == 0) || (ti == 0);
-            const bool last = (j == (int)n - 1) || (ti == nt - 1);
+            const bool last = (j == n - 1) || (ti == nt - 1);
             if (first) {
-                // -------- segment prologue (both groups): queries, operand scales, row state
                 ++seg;
                 seg_u = u;
-                const int layer = (int)(u / P.p.H), kvh = (int)(u % P.p.H);
-                uint4 qv[4];
-                float qm = 0.0f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int cid = si + 256 * m;
-                    qv[m] = make_uint4(0u, 0u, 0u, 0u);
-                    if (cid < R * 16) {
-                        const int r = cid >> 4, dc = cid & 15;
-                        const int a = r / P.G, gq = r % P.G;
-                        qv[m] = __ldg(reinterpret_cast<const uint4*>(
-                                          P.q + (((int64_t)layer * P.A + a) * P.Hq + kvh * P.G + gq) * kD) + dc);
-                        const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float lo, hi;
-                            if (QBF16) {
-                                lo = __uint_as_float(wv[e] << 16);
-                                hi = __uint_as_float(wv[e] & 0xFFFF0000u);
-                            } else {
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-                                lo = f.x;
-                                hi = f.y;
-                            }
-                            qm = fmaxf(qm, fmaxf(fabsf(lo), fabsf(hi)));
-                        }
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
-                if (lane == 0) M.qred[warp - 4] = qm;
-                tc::named_bar(3, 256);
-                float qmax = 0.0f;
-#pragma unroll
-                for (int w8 = 0; w8 < 8; ++w8) qmax = fmaxf(qmax, M.qred[w8]);
-                int eq = 0;
-                if (qmax > 0.0f) frexpf(qmax, &eq);
-                const float fq = qmax > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;  // qmax * fq in [2^14, 2^15)
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int cid = si + 256 * m;
-                    if (cid < kNR * 16) {
-                        const int r = cid >> 4, dc = cid & 15;
-                        const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
-                        uint32_t hv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float lo = 0.0f, hi = 0.0f;
-                            if (r < R) {
-                                if (QBF16) {
-                                    lo = __uint_as_float(wv[e] << 16);
-                                    hi = __uint_as_float(wv[e] & 0xFFFF0000u);
-                                } else {
-                                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-                                    lo = f.x;
-                                    hi = f.y;
-                                }
-                            }
-                            const __half2 h = __floats2half2_rn(lo * fq, hi * fq);
-                            hv[e] = *reinterpret_cast<const uint32_t*>(&h);
-                        }
-                        *reinterpret_cast<uint4*>(sQ + (dc >> 3) * 8192 + tc::sw128(r, (dc & 7) * 16)) =
-                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                    }
-                }
-                if (si == 0) {
-                    const float nmax = P.p.nmax[u];
-                    int en = 0;
-                    if (nmax > 0.0f) frexpf(nmax, &en);
-                    M.scale_eff = P.scale_log2 * 16.0f / fq;  // keys are stored in TMEM as s * code * 2^-4
-                    M.wscale = nmax > 0.0f ? ldexpf(1.0f, 8 - en) : 1.0f;  // ||v|| * wscale < 2^8
-                }
-                if (si < kNR) M.msm[si] = si < R ? -INFINITY : INFINITY;
-                tc::fence_proxy_async();
-                tc::named_bar(3, 256);
-                if (si == 0) tc::mbar_arrive(tc::smem_u32(&M.qready));
+                softmax_prologue<QBF16>(P.q, P.p.nmax, u, P.p.H, P.A, P.Hq, P.G, P.R, P.scale_log2, sQ, M, si, warp - 8,
+                                        lane);
             }
             const float scale_eff = M.scale_eff;
-            const float wscale = M.wscale;
-            const int64_t tok = (int64_t)ti * kTile + tt;
-            const bool valid = tok < P.n_ctx;
-            // per-token norm from the ring (after an abort the waits return at once and the loop runs to the
-            // end with garbage, so both row groups pass the same named barriers)
-            tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs);
-            const unsigned short nb = *reinterpret_cast<const unsigned short*>(sR + st * kRawStage + kRawN + tt * 2);
-            tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
-            const float wt = valid ? __half2float(__ushort_as_half(nb)) * wscale : 0.0f;
-            // -------- logits: x = scale_eff * (q' . k_hat) for this group's 32 rows
-            float2 x2[16];
-            tc::mbar_wait(tc::smem_u32(&M.sfull[s]), ph, abortp, kTimeoutNs);
-            tc::fence_after();
-            {
-                uint32_t t0[16], t1[16];
-                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase, t0);
-                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase + 16u, t1);
+            const bool tail = (int64_t)(ti + 1) * kTile > P.n_ctx;
+            const bool valid = (int64_t)ti * kTile + tt < P.n_ctx;
+            // -------- logits for this group's 32 rows, d = c * S - m, recomputed from TMEM in each pass
+            // (absolute c * S on a segment's first tile, before the running max exists)
+            const float2 c2 = make_float2(scale_eff, scale_eff);
+            auto logits16 = [&](int cc, float2 (&d2)[8], bool absolute) {
+                uint32_t t0[16];
+                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase + 16u * cc, t0);
                 tc::wait_ld();
-                const float2 c2 = make_float2(scale_eff, scale_eff);
+                const float2* nm2 = reinterpret_cast<const float2*>(&M.nm[rbase + 16 * cc]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    x2[k] = mul2(c2, make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1])));
-                    x2[8 + k] = mul2(c2, make_float2(__uint_as_float(t1[2 * k]), __uint_as_float(t1[2 * k + 1])));
+                    const float2 sv = make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1]));
+                    d2[k] = absolute ? mul2(c2, sv) : fma2(c2, sv, nm2[k]);
                 }
-            }
-            tc::fence_before();
-            tc::mbar_arrive(tc::smem_u32(&M.sfree[s]));
-            if (!valid) {
+                if (tail && !valid) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) x2[k] = make_float2(-INFINITY, -INFINITY);
-            }
-            // -------- lazy rescale decision (per row group); rows >= R carry m = +inf
-            const float2* msm2 = reinterpret_cast<const float2*>(&M.msm[rbase]);
-            float dmax = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float2 d = sub2(x2[k], msm2[k]);
-                dmax = fmaxf(dmax, fmaxf(d.x, d.y));
-            }
-            if (tt == 0) M.flags[grp][f3 == 2 ? 0 : f3 + 1] = 0;
-            if (__any_sync(0xffffffffu, dmax > kTau) && lane == 0) atomicOr(&M.flags[grp][f3], 1);
-            tc::named_bar(gbar, 128);
-            if (M.flags[grp][f3]) {
-                // tile maximum of every row of this group (warp reduction per row, then across warps)
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float v0 = tc::warp_max(x2[k].x);
-                    const float v1 = tc::warp_max(x2[k].y);
-                    if (lane == 2 * k) M.red[grp][wq][2 * k] = v0;
-                    if (lane == 2 * k + 1) M.red[grp][wq][2 * k + 1] = v1;
+                    for (int k = 0; k < 8; ++k) d2[k] = make_float2(-INFINITY, -INFINITY);
                 }
-                softmax_rescale(M, grp, wq, tt, rbase, gbar, first, j, lane_addr, abortp);
+            };
+            tc::mbar_wait(tc::smem_u32(&M.sfull[s]), ph, abortp, kTimeoutNs);
+            tc::fence_after();
+            // -------- lazy rescale: only when some logit exceeds the running max by more than 2^tau
+            bool need = first;
+            if (!first) {
+                float dmax = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float2 d2[8];
+                    logits16(cc, d2, false);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) dmax = fmaxf(dmax, fmaxf(d2[k].x, d2[k].y));
+                }
+                // ids 4, 5: a reducing barrier never shares its id with the bar.sync barriers (1, 2)
+                need = bar_any(gbar + 3, 128, dmax > kTau);
             }
-            // -------- probabilities, running sums, P' = p * ||v|| * wscale (fp16), stored as produced
+            if (need) {
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float2 d2[8];
+                    logits16(cc, d2, first);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float v0 = tc::warp_max(d2[k].x);
+                        const float v1 = tc::warp_max(d2[k].y);
+                        if (lane == 16 * cc + 2 * k) M.red[grp][wq][16 * cc + 2 * k] = v0;
+                        if (lane == 16 * cc + 2 * k + 1) M.red[grp][wq][16 * cc + 2 * k + 1] = v1;
+                    }
+                }
+                softmax_new_max(M, grp, tt, rbase, R, gbar, first, j, lane_addr, abortp);
+            }
+            // -------- probabilities p = 2^d (fp16) and running sums, against the (new) running max
             if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
-            uint8_t* prow = sP + s * 16384;
-            const float2 wt2 = make_float2(wt, wt);
+            const uint32_t prow = tc::smem_u32(sP) + s * 16384;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t tl[16];
                 if (!first) tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
+                float2 d2[8];
+                logits16(cc, d2, false);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int k = 8 * cc + 4 * half + e;
-                        const float2 d = sub2(x2[k], msm2[k]);
-                        x2[k] = make_float2(ex2(d.x), ex2(d.y));  // x2 now holds p
-                        const float2 pw = mul2(x2[k], wt2);
-                        const __half2 h = __floats2half2_rn(pw.x, pw.y);
+                        const int k = 4 * half + e;
+                        d2[k] = make_float2(ex2(d2[k].x), ex2(d2[k].y));  // d2 now holds p
+                        const __half2 h = __floats2half2_rn(d2[k].x, d2[k].y);
                         pk[e] = *reinterpret_cast<const uint32_t*>(&h);
                     }
-                    *reinterpret_cast<uint4*>(prow + tc::sw128((uint32_t)tt, 16u * (4 * grp + 2 * cc + half))) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    st_shared16(prow + tc::sw128((uint32_t)tt, 16u * (4 * grp + 2 * cc + half)), pk[0], pk[1], pk[2],
+                                pk[3]);
                 }
-                if (!first) tc::wait_ld();
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const float2 p = x2[8 * cc + k];
                     float2 l = first ? make_float2(0.0f, 0.0f)
                                      : make_float2(__uint_as_float(tl[2 * k]), __uint_as_float(tl[2 * k + 1]));
-                    l = add2(l, p);
+                    l = add2(l, d2[k]);
                     tl[2 * k] = __float_as_uint(l.x);
                     tl[2 * k + 1] = __float_as_uint(l.y);
                 }
                 tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
             }
-            tc::fence_proxy_async();
             tc::fence_before();
+            tc::mbar_arrive(tc::smem_u32(&M.sfree[s]));   // S has been read for the last time
+            tc::fence_proxy_async();
             tc::mbar_arrive(tc::smem_u32(&M.pfull[s]));
 
             if (last) {
-                // -------- segment epilogue: row sums, O^T, partial for (unit, piece)
-                tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph, abortp, kTimeoutNs);
-                tc::fence_after();
-                tc::wait_st();
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t tl[16];
-                    tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float v = __uint_as_float(tl[k]);
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                        if (lane == 16 * cc + k) M.red[grp][wq][16 * cc + k] = v;
-                    }
-                }
-                tc::named_bar(gbar, 128);
                 const int64_t ulo = cta_of_tile(seg_u * nt, TT, P.nctas);
-                const int64_t slot = seg_u * P.pmax + (c - ulo);
-                const float unscale = 1.0f / wscale;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t to[16];
-                    tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int r = rbase + 16 * cc + k;
-                        if (r < R) P.ws_acc[(slot * R + r) * kD + tt] = __uint_as_float(to[k]) * unscale;
-                    }
-                }
-                if (tt < 32 && rbase + tt < R) {
-                    const int r = rbase + tt;
-                    P.ws_ml[(slot * R + r) * 2] = M.msm[r];
-                    P.ws_ml[(slot * R + r) * 2 + 1] =
-                        M.red[grp][0][tt] + M.red[grp][1][tt] + M.red[grp][2][tt] + M.red[grp][3][tt];
-                }
-                tc::fence_before();
-                tc::named_bar(3, 256);
+                softmax_epilogue(M, s, ph, abortp, lane_addr, grp, wq, lane, tt, rbase, R, gbar,
+                                 seg_u * P.pmax + (c - ulo), P.ws_acc, P.ws_ml);
             }
         }
-    } else if (warp == 12 && lane == 0) {
-        // =============================== MMA issuer (one thread)
+    } else if (warp == 16 && lane == 0) {
+        // =============================== MMA issuer (one thread): an event loop over both chains
         const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);
         const uint32_t id2 = tc::idesc_f16(128, kNR, true, true);
         const uint32_t sq = tc::smem_u32(sQ), sv = tc::smem_u32(sV), sp = tc::smem_u32(sP);
-        auto issue_mma2 = [&](int jj, bool seg_first) -> bool {
-            const int s2 = jj & 1;
-            const uint32_t ph2 = (uint32_t)((jj >> 1) & 1);
-            if (!tc::mbar_wait(tc::smem_u32(&M.vfull[s2]), ph2, abortp, kTimeoutNs, false)) return false;
-            if (!tc::mbar_wait(tc::smem_u32(&M.pfull[s2]), ph2, abortp, kTimeoutNs, false)) return false;
-            tc::fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = tc::sdesc(sv + s2 * 32768 + ks * 2048, 16384, 1024);
-                const uint64_t bd = tc::sdesc(sp + s2 * 16384 + ks * 2048, 16384, 1024);
-                tc::mma_ss(tbase + kColO, ad, bd, id2, (seg_first && ks == 0) ? 0u : 1u);
-            }
-            tc::commit(tc::smem_u32(&M.pvfree[s2]));
-            return true;
-        };
-        int seg = -1;
+        int j1 = 0, j2 = 0;        // next MMA1 / MMA2 tile
+        int seg1 = 0;              // segments whose first MMA1 has been issued
+        int ti1 = (int)(g0 % nt), ti2 = ti1;
         bool ok = P.test_stall == 0;
-        int ti = (int)(g0 % nt) - 1;
-        bool prev_first = false;
-        for (int j = 0; j < (int)n && ok; ++j) {
-            if (++ti == nt) ti = 0;
-            const bool first = (j == 0) || (ti == 0);
-            const int s = j & 1;
-            const uint32_t ph = (uint32_t)((j >> 1) & 1);
-            if (first) {
-                if (j > 0 && !issue_mma2(j - 1, prev_first)) break;
-                ++seg;
-                if (!tc::mbar_wait(tc::smem_u32(&M.qready), (uint32_t)(seg & 1), abortp, kTimeoutNs, false)) break;
-            }
-            if (!tc::mbar_wait(tc::smem_u32(&M.kfull[s]), ph, abortp, kTimeoutNs, false)) break;
-            if (j >= 2 &&
-                !tc::mbar_wait(tc::smem_u32(&M.sfree[s]), (uint32_t)(((j - 2) >> 1) & 1), abortp, kTimeoutNs, false))
-                break;
-            tc::fence_after();
+        uint64_t t_last = tc::globaltimer();
+        while (ok && j2 < n) {
+            bool prog = false;
+            if (j1 < n) {
+                const int s = j1 & 1;
+                const bool f1 = (j1 == 0) || (ti1 == 0);
+                if ((!f1 || tc::mbar_try(tc::smem_u32(&M.qready), (uint32_t)(seg1 & 1))) &&
+                    tc::mbar_try(tc::smem_u32(&M.kfull[s]), (uint32_t)((j1 >> 1) & 1)) &&
+                    (j1 < 2 || tc::mbar_try(tc::smem_u32(&M.sfree[s]), (uint32_t)(((j1 - 2) >> 1) & 1)))) {
+                    tc::fence_after();
 #pragma unroll
-            for (int part = 0; part < 2; ++part)   // hi then lo halves of the scaled keys
+                    for (int part = 0; part < 2; ++part)   // hi then lo halves of the scaled keys
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t bd = tc::sdesc(sq + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
-                    tc::mma_ts(tbase + kColS + 64u * s, tbase + kColK + 128u * s + 64u * part + 8u * ks, bd, id1,
-                               (part | ks) ? 1u : 0u);
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t bd = tc::sdesc(sq + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
+                            tc::mma_ts(tbase + kColS + 64u * s, tbase + kColK + 128u * s + 64u * part + 8u * ks, bd,
+                                       id1, (part | ks) ? 1u : 0u);
+                        }
+                    tc::commit(tc::smem_u32(&M.sfull[s]));
+                    tc::commit(tc::smem_u32(&M.kfree[s]));
+                    if (f1) ++seg1;
+                    if (++ti1 == nt) ti1 = 0;
+                    ++j1;
+                    prog = true;
                 }
-            tc::commit(tc::smem_u32(&M.sfull[s]));
-            tc::commit(tc::smem_u32(&M.kfree[s]));
-            if (!first) ok = issue_mma2(j - 1, prev_first);
-            prev_first = first;
+            }
+            if (j2 < j1) {
+                const int s2 = j2 & 1;
+                const uint32_t ph2 = (uint32_t)((j2 >> 1) & 1);
+                if (tc::mbar_try(tc::smem_u32(&M.vfull[s2]), ph2) && tc::mbar_try(tc::smem_u32(&M.pfull[s2]), ph2)) {
+                    const bool f2 = (j2 == 0) || (ti2 == 0);
+                    tc::fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = tc::sdesc(sv + s2 * 32768 + ks * 2048, 16384, 1024);
+                        const uint64_t bd = tc::sdesc(sp + s2 * 16384 + ks * 2048, 16384, 1024);
+                        tc::mma_ss(tbase + kColO, ad, bd, id2, (f2 && ks == 0) ? 0u : 1u);
+                    }
+                    tc::commit(tc::smem_u32(&M.pvfree[s2]));
+                    if (++ti2 == nt) ti2 = 0;
+                    ++j2;
+                    prog = true;
+                }
+            }
+            if (prog) {
+                t_last = tc::globaltimer();
+            } else {
+                if (*abortp) break;
+                if (tc::globaltimer() - t_last > kTimeoutNs) {
+                    *abortp = 1;
+                    break;
+                }
+            }
         }
-        if (ok && n > 0 && !*abortp) issue_mma2((int)n - 1, prev_first);
         if (P.test_stall) *abortp = 0;  // let the other roles discover the stall on their own waits
-        if (n > 0) {
+        if (j1 > 0) {
             // every MMA this thread issued must have completed before the TMEM is freed
             tc::commit(tc::smem_u32(&M.done));
             volatile int dummy = 0;
@@ -709,7 +806,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ---- tear-down: every role is past its last TMEM access
     tc::fence_before();
     __syncthreads();
-    if (warp == 12) {
+    if (warp == 16) {
         tc::fence_after();
         tc::tmem_dealloc(tbase, kTmemCols);
     }
