@@ -161,13 +161,25 @@ typedef struct {
     const void* suffix_k;
     const void* suffix_v;
     int64_t suffix_len;
+    /* Query-chunk mode: each agent brings chunk_len query tokens, each with its own key and value
+     * (in_dtype bits, chunk_k / chunk_v [n_layers][n_agents][n_kv_heads][chunk_len][head_dim]
+     * contiguous, device, 16-byte aligned). Query token c of an agent attends the whole pool plus
+     * that agent's chunk tokens 0..c (causal inside the chunk), under one softmax. q and out are then
+     * [n_layers][n_agents][chunk_len][n_q_heads][head_dim]. chunk_len = 0 disables it; it cannot be
+     * combined with a suffix. At most 16 query heads per kv head. */
+    const void* chunk_k;
+    const void* chunk_v;
+    int64_t chunk_len;
 } polykv_attend_ext;
 
 /* Workspace bytes for polykv_attend_ex with these arguments (ext may be NULL). */
 POLYKV_API polykv_status polykv_attend_ex_workspace_size(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads,
                                                          int64_t n_ctx, const polykv_attend_ext* ext, size_t* bytes);
 
-/* polykv_attend with extensions. With a suffix the output is
+/* polykv_attend with extensions. In chunk mode the output for query token c of agent a is
+ *   out[l][a][c][hq] = sum over pool tokens t < n_ctx and chunk tokens c' <= c of softmax(scale * q.k) v
+ * (the agent's chunk keys/values used as given); E_UNSUPPORTED if a suffix is also given.
+ * With a suffix the output is
  *   out[l][a][hq] = sum over pool tokens t < n_ctx and suffix tokens s of softmax(scale * q.k) v
  * where pool keys/values are dequantized as in polykv_attend and suffix keys/values are used as
  * given. Errors as polykv_attend, plus E_INVAL for a bad suffix and E_UNSUPPORTED for more than 16

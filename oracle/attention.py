@@ -82,13 +82,15 @@ def dequantize_pool_layer(k_codes, k_scales, v_codes, v_norms, centroids_f32):
 
 
 def attend_pool(q_bits, dtype, pool, n_ctx, centroids_f32, scale=None, layers=None,
-                suffix_k_bits=None, suffix_v_bits=None):
+                suffix_k_bits=None, suffix_v_bits=None, chunk_k_bits=None, chunk_v_bits=None):
     """Reference output for a whole pool.
 
     q_bits: uint16 [L][A][Hq][d] (fp16/bf16 bit patterns); pool: dict with
     unpacked fields 'k_codes' [L][H][>=n_ctx][d] int8, 'k_scales' fp16,
     'v_codes' uint8 [L][H][>=n_ctx][d], 'v_norms' fp16 [L][H][>=n_ctx].
-    Returns float64 [len(layers)][A][Hq][d]."""
+    Returns float64 [len(layers)][A][Hq][d].
+    Query-chunk mode (chunk_k_bits/chunk_v_bits [L][A][H][C][d]): q_bits is
+    [L][A][C][Hq][d] and the result [len(layers)][A][C][Hq][d]."""
     L = q_bits.shape[0]
     d = q_bits.shape[-1]
     scale = (1.0 / np.sqrt(d)) if scale is None else scale
@@ -99,6 +101,12 @@ def attend_pool(q_bits, dtype, pool, n_ctx, centroids_f32, scale=None, layers=No
                                        pool["v_codes"][l, :, :n_ctx], pool["v_norms"][l, :, :n_ctx],
                                        centroids_f32)
         q = _keys.bits_to_f32(q_bits[l], dtype).astype(np.float64)
+        if chunk_k_bits is not None:
+            # [A][H][C][d] -> [A][C][H][d] as attend_chunk_layer takes it
+            ck = _keys.bits_to_f32(chunk_k_bits[l], dtype).astype(np.float64).transpose(0, 2, 1, 3)
+            cv = _keys.bits_to_f32(chunk_v_bits[l], dtype).astype(np.float64).transpose(0, 2, 1, 3)
+            outs.append(attend_chunk_layer(q, kh, vh, scale, ck, cv))
+            continue
         sk = sv = None
         if suffix_k_bits is not None:
             sk = _keys.bits_to_f32(suffix_k_bits[l], dtype).astype(np.float64)

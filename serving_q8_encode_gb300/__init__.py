@@ -43,7 +43,8 @@ class PoolRegions(ctypes.Structure):
 
 
 class AttendExt(ctypes.Structure):
-    _fields_ = [("suffix_k", ctypes.c_void_p), ("suffix_v", ctypes.c_void_p), ("suffix_len", ctypes.c_int64)]
+    _fields_ = [("suffix_k", ctypes.c_void_p), ("suffix_v", ctypes.c_void_p), ("suffix_len", ctypes.c_int64),
+                ("chunk_k", ctypes.c_void_p), ("chunk_v", ctypes.c_void_p), ("chunk_len", ctypes.c_int64)]
 
 
 _lib = None
@@ -243,6 +244,25 @@ class Pool:
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
         polykv_attend_ex(self.handle, q.data_ptr(), out.data_ptr(), A, Hq, n_ctx, softmax_scale, ext, ws.data_ptr(),
                          ws.numel(), _stream_handle(stream))
+        return out
+
+    def attend_chunk(self, q, n_ctx: int, chunk_k, chunk_v, out=None, softmax_scale: float = 0.0, stream=None,
+                     workspace=None):
+        """Query-chunk mode: q device [L][A][C][Hq][d]; chunk_k/v device [L][A][H][C][d] (pool dtype
+        bits, contiguous). Query token c of agent a sees the pool plus that agent's chunk tokens 0..c.
+        Returns fp32 [L][A][C][Hq][d]."""
+        import torch
+        L, A, C, Hq, d = q.shape
+        assert q.is_contiguous() and chunk_k.is_contiguous() and chunk_v.is_contiguous()
+        assert chunk_k.shape == chunk_v.shape and chunk_k.shape[3] == C
+        ext = AttendExt(chunk_k=chunk_k.data_ptr(), chunk_v=chunk_v.data_ptr(), chunk_len=C)
+        if out is None:
+            out = torch.empty((L, A, C, Hq, d), dtype=torch.float32, device=q.device)
+        need = polykv_attend_ex_workspace_size(self.handle, A, Hq, n_ctx, ext)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        polykv_attend_ex(self.handle, q.data_ptr(), out.data_ptr(), A, Hq, n_ctx, softmax_scale, ext,
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
         return out
 
     # -- views of the encoded fields (for inspection and tests)

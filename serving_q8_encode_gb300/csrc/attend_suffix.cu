@@ -1,5 +1,6 @@
-// Private per-agent suffix of uncompressed keys/values, attended together with
-// the shared compressed pool under ONE softmax.
+// Private per-agent keys/values attended together with the shared compressed pool under ONE
+// softmax: a suffix of uncompressed recent tokens, or (query-chunk mode) a chunk of query tokens
+// that each carry their own key/value, seen causally.
 //
 // Each agent appends its own recent tokens after the shared context; those
 // are not part of the compressed pool (the PolyKV abstract's pool is the shared
@@ -140,6 +141,151 @@ __global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __
     }
 }
 
+// ---------------------------------------------------------------- query-chunk mode
+// Each agent's chunk of C query tokens carries its own keys/values; query token c sees the agent's
+// chunk tokens 0..c (plus the pool, merged later). One block per (layer, agent, kv head, block of 32
+// query rows r = c * G + g); chunk keys/values go through shared memory in tiles of 64 tokens; one
+// warp owns 8 rows (one online-softmax state each), a lane one token of the tile for the scores and
+// D/32 head dims for the accumulator. The partial (running max in log2 units, sum, unnormalised
+// accumulator in the original basis) goes to the same slots as a suffix partial, with the chunk
+// position folded into the agent index (a' = a * C + c).
+constexpr int kChT = 64;
+constexpr int kChRows = 32;
+constexpr int kChThreads = 128;
+
+template <int D>
+constexpr size_t chunk_smem_bytes() {
+    return sizeof(float) * ((size_t)kChT * (D + 1) + (size_t)kChT * D + (size_t)kChRows * D + 4 * kChT);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kChThreads) chunk_partial(const uint16_t* __restrict__ q,
+                                                            const uint16_t* __restrict__ ck,
+                                                            const uint16_t* __restrict__ cv, int H, int Hq, int64_t C,
+                                                            float scale_log2, float* __restrict__ acc_out,
+                                                            float* __restrict__ ml_out) {
+    extern __shared__ float chs[];
+    float* Ks = chs;                       // [kChT][D + 1]
+    float* Vs = Ks + kChT * (D + 1);       // [kChT][D]
+    float* Qs = Vs + kChT * D;             // [kChRows][D]
+    float* Ps = Qs + kChRows * D;          // [4 warps][kChT]
+    constexpr int RW = kChRows / 4;        // rows per warp
+    constexpr int DPL = D / 32;            // accumulator dims per lane
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = Hq / H;
+    const int64_t unit = blockIdx.x;       // (layer * A + a) * H + h
+    const int h = (int)(unit % H);
+    const int64_t la = unit / H;           // layer * A + a
+    const int64_t rows = C * G;
+    const int64_t r0 = (int64_t)blockIdx.y * kChRows;
+    const uint16_t* kb = ck + unit * C * D;
+    const uint16_t* vb = cv + unit * C * D;
+
+    for (int i = tid; i < kChRows * D; i += kChThreads) {
+        const int64_t r = r0 + i / D;
+        float x = 0.0f;
+        if (r < rows) {
+            const int64_t c = r / G;
+            const int g = (int)(r % G);
+            x = bits_to_float(q[((la * C + c) * Hq + h * G + g) * D + i % D], BF16);
+        }
+        Qs[i] = x;
+    }
+    float m[RW], l[RW], acc[RW][DPL];
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[i][e] = 0.0f;
+    }
+    const int64_t r_last = (r0 + kChRows < rows ? r0 + kChRows : rows) - 1;
+    const int64_t c_max = r_last / G;
+    for (int64_t t0 = 0; t0 <= c_max; t0 += kChT) {
+        __syncthreads();
+        for (int i = tid; i < kChT * D; i += kChThreads) {
+            const int tk = i / D, dd = i % D;
+            const bool ok = t0 + tk < C;
+            Ks[tk * (D + 1) + dd] = ok ? bits_to_float(kb[(t0 + tk) * D + dd], BF16) : 0.0f;
+            Vs[tk * D + dd] = ok ? bits_to_float(vb[(t0 + tk) * D + dd], BF16) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            const int ri = warp * RW + i;
+            const int64_t r = r0 + ri;
+            if (r >= rows) continue;               // warp-uniform
+            const int64_t c = r / G;
+            if (t0 > c) continue;                  // no visible token in this tile (warp-uniform)
+            const float* qr = Qs + ri * D;
+            float x0 = 0.0f, x1 = 0.0f;
+#pragma unroll 8
+            for (int dd = 0; dd < D; ++dd) {
+                x0 = fmaf(qr[dd], Ks[lane * (D + 1) + dd], x0);
+                x1 = fmaf(qr[dd], Ks[(lane + 32) * (D + 1) + dd], x1);
+            }
+            x0 = (t0 + lane <= c) ? x0 * scale_log2 : -INFINITY;
+            x1 = (t0 + lane + 32 <= c) ? x1 * scale_log2 : -INFINITY;
+            float tmax = fmaxf(x0, x1);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+            const float mn = fmaxf(m[i], tmax);
+            const float alpha = m[i] == -INFINITY ? 0.0f : exp2f(m[i] - mn);
+            const float p0 = exp2f(x0 - mn), p1 = exp2f(x1 - mn);
+            float ps = p0 + p1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            l[i] = l[i] * alpha + ps;
+            m[i] = mn;
+            Ps[warp * kChT + lane] = p0;
+            Ps[warp * kChT + lane + 32] = p1;
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[i][e] *= alpha;
+            const int tmaxk = (int)((c - t0 + 1) < kChT ? (c - t0 + 1) : kChT);
+            for (int tk = 0; tk < tmaxk; ++tk) {
+                const float pp = Ps[warp * kChT + tk];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[i][e] = fmaf(pp, Vs[tk * D + lane * DPL + e], acc[i][e]);
+            }
+            __syncwarp();
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        const int64_t r = r0 + warp * RW + i;
+        if (r >= rows) continue;
+        const int64_t c = r / G;
+        const int g = (int)(r % G);
+        const int64_t orow = (la * C + c) * Hq + h * G + g;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc_out[orow * D + lane * DPL + e] = acc[i][e];
+        if (lane == 0) {
+            ml_out[orow * 2] = m[i];
+            ml_out[orow * 2 + 1] = l[i];
+        }
+    }
+}
+
+template <int D, bool BF16>
+polykv_status run_chunk(const SuffixArgs& a, int L, int A_virtual, int H, int Hq, float scale, cudaStream_t st) {
+    const int G = Hq / H;
+    const int64_t C = a.chunk;
+    const int64_t A = A_virtual / C;
+    const int64_t nblk_rows = (C * G + kChRows - 1) / kChRows;
+    if (nblk_rows > 65535) return set_error(POLYKV_E_UNSUPPORTED, "chunk: %lld query rows per kv head", (long long)(C * G));
+    const dim3 grid((unsigned)((int64_t)L * A * H), (unsigned)nblk_rows);
+    constexpr size_t smem = chunk_smem_bytes<D>();
+    cudaError_t e = cudaFuncSetAttribute(chunk_partial<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "chunk: smem attribute: %s", cudaGetErrorString(e));
+    chunk_partial<D, BF16><<<grid, kChThreads, smem, st>>>(
+        static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), static_cast<const uint16_t*>(a.v), H, Hq,
+        C, scale * 1.4426950408889634f, a.acc, a.ml);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "chunk launch: %s", cudaGetErrorString(e));
+    return POLYKV_OK;
+}
+
 template <int D, bool BF16>
 polykv_status run_suffix(const SuffixArgs& a, int L, int A, int H, int Hq, float scale, cudaStream_t st) {
     const int G = Hq / H;
@@ -163,6 +309,11 @@ polykv_status run_suffix(const SuffixArgs& a, int L, int A, int H, int Hq, float
 polykv_status launch_attend_suffix(const SuffixArgs& a, polykv_dtype dt, int L, int A, int H, int Hq, int D,
                                    float scale, cudaStream_t st) {
     const bool bf = dt == POLYKV_BF16;
+    if (a.chunk > 0) {
+        if (D == 128) return bf ? run_chunk<128, true>(a, L, A, H, Hq, scale, st) : run_chunk<128, false>(a, L, A, H, Hq, scale, st);
+        if (D == 64) return bf ? run_chunk<64, true>(a, L, A, H, Hq, scale, st) : run_chunk<64, false>(a, L, A, H, Hq, scale, st);
+        return set_error(POLYKV_E_UNSUPPORTED, "chunk: head_dim %d", D);
+    }
     if (D == 128) return bf ? run_suffix<128, true>(a, L, A, H, Hq, scale, st) : run_suffix<128, false>(a, L, A, H, Hq, scale, st);
     if (D == 64) return bf ? run_suffix<64, true>(a, L, A, H, Hq, scale, st) : run_suffix<64, false>(a, L, A, H, Hq, scale, st);
     return set_error(POLYKV_E_UNSUPPORTED, "suffix: head_dim %d", D);

@@ -278,14 +278,32 @@ static size_t suffix_bytes(const polykv_pool* pool, int32_t n_agents, int32_t n_
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Query-chunk mode runs the pool part with the chunk position folded into the agent index
+// (agents x chunk_len "virtual agents", the same row layout as q [L][A][C][Hq][d]).
+static polykv_status chunk_agents(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads,
+                                  const polykv_attend_ext* ext, int64_t* agents) {
+    if (ext->suffix_len != 0) return set_error(POLYKV_E_UNSUPPORTED, "chunk mode cannot be combined with a suffix");
+    if (ext->chunk_len < 0) return set_error(POLYKV_E_INVAL, "chunk_len must be >= 0");
+    const int64_t av = (int64_t)n_agents * ext->chunk_len;
+    if (av * (n_q_heads / pool->desc.n_kv_heads) > (1 << 20))
+        return set_error(POLYKV_E_UNSUPPORTED, "chunk mode: too many query rows per kv head");
+    *agents = av;
+    return POLYKV_OK;
+}
+
 polykv_status polykv_attend_ex_workspace_size(const polykv_pool* pool, int32_t n_agents, int32_t n_q_heads,
                                               int64_t n_ctx, const polykv_attend_ext* ext, size_t* bytes) {
     const polykv_status st = check_attend_args(pool, n_agents, n_q_heads, n_ctx);
     if (st != POLYKV_OK) return st;
     if (!bytes) return set_error(POLYKV_E_INVAL, "bytes is NULL");
-    const int rows = n_agents * (n_q_heads / pool->desc.n_kv_heads);
+    int64_t agents = n_agents;
+    if (ext && ext->chunk_len != 0) {
+        const polykv_status cs = chunk_agents(pool, n_agents, n_q_heads, ext, &agents);
+        if (cs != POLYKV_OK) return cs;
+    }
+    const int rows = (int)(agents * (n_q_heads / pool->desc.n_kv_heads));
     size_t b = attend_workspace(pool->view, rows, n_ctx);
-    if (ext && ext->suffix_len > 0) b = align256(b) + suffix_bytes(pool, n_agents, n_q_heads);
+    if (ext && (ext->suffix_len > 0 || ext->chunk_len > 0)) b = align256(b) + suffix_bytes(pool, (int32_t)agents, n_q_heads);
     *bytes = b;
     return POLYKV_OK;
 }
@@ -293,11 +311,43 @@ polykv_status polykv_attend_ex_workspace_size(const polykv_pool* pool, int32_t n
 polykv_status polykv_attend_ex(const polykv_pool* pool, const void* q, float* out, int32_t n_agents,
                                int32_t n_q_heads, int64_t n_ctx, float softmax_scale, const polykv_attend_ext* ext,
                                void* workspace, size_t workspace_bytes, void* stream) {
-    if (!ext || ext->suffix_len == 0)
+    if (!ext || (ext->suffix_len == 0 && ext->chunk_len == 0))
         return polykv_attend(pool, q, out, n_agents, n_q_heads, n_ctx, softmax_scale, workspace, workspace_bytes,
                              stream);
     const polykv_status st = check_attend_args(pool, n_agents, n_q_heads, n_ctx);
     if (st != POLYKV_OK) return st;
+    if (ext->chunk_len != 0) {
+        int64_t av = 0;
+        const polykv_status cs = chunk_agents(pool, n_agents, n_q_heads, ext, &av);
+        if (cs != POLYKV_OK) return cs;
+        if (!q || !out || !workspace) return set_error(POLYKV_E_INVAL, "q, out and workspace must be non-NULL");
+        if (!aligned16(q) || !aligned16(out) || !aligned16(workspace))
+            return set_error(POLYKV_E_INVAL, "q, out and workspace must be 16-byte aligned");
+        if (!ext->chunk_k || !ext->chunk_v || !aligned16(ext->chunk_k) || !aligned16(ext->chunk_v))
+            return set_error(POLYKV_E_INVAL, "chunk_k and chunk_v must be non-NULL and 16-byte aligned");
+        if (n_q_heads / pool->desc.n_kv_heads > 16)
+            return set_error(POLYKV_E_UNSUPPORTED, "chunk: more than 16 query heads per kv head");
+        const int rows = (int)(av * (n_q_heads / pool->desc.n_kv_heads));
+        const size_t pool_ws = attend_workspace(pool->view, rows, n_ctx);
+        const size_t need = align256(pool_ws) + suffix_bytes(pool, (int32_t)av, n_q_heads);
+        if (workspace_bytes < need)
+            return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend_ex: workspace %zu < %zu bytes", workspace_bytes, need);
+        const size_t nrows = (size_t)pool->desc.n_layers * (size_t)av * (size_t)n_q_heads;
+        SuffixArgs chk;
+        chk.q = q;
+        chk.k = ext->chunk_k;
+        chk.v = ext->chunk_v;
+        chk.len = ext->chunk_len;
+        chk.chunk = ext->chunk_len;
+        chk.acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(pool_ws));
+        chk.ml = chk.acc + nrows * (size_t)pool->desc.head_dim;
+        const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
+        if (use_tc_path(pool->view, rows))
+            return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, (int)av, n_q_heads, n_ctx, scale,
+                                    workspace, pool_ws, static_cast<cudaStream_t>(stream), &chk);
+        return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, (int)av, n_q_heads, n_ctx, scale,
+                                  workspace, pool_ws, static_cast<cudaStream_t>(stream), &chk);
+    }
     if (!q || !out || !workspace) return set_error(POLYKV_E_INVAL, "q, out and workspace must be non-NULL");
     if (!aligned16(q) || !aligned16(out) || !aligned16(workspace))
         return set_error(POLYKV_E_INVAL, "q, out and workspace must be 16-byte aligned");

@@ -50,6 +50,7 @@ struct SuffixArgs {
     int64_t len;
     float* acc;
     float* ml;
+    int64_t chunk = 0;   // > 0: query-chunk mode (len = chunk, causal; the attend's n_agents counts agents x chunk)
 };
 polykv_status launch_attend_suffix(const SuffixArgs& a, polykv_dtype dt, int L, int A, int H, int Hq, int D,
                                    float scale, cudaStream_t st);

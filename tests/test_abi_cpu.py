@@ -123,3 +123,16 @@ def test_call_order_and_argument_errors_before_launch(lib):
 
 def test_free_null_is_ok(lib):
     pk.polykv_free(None)
+
+
+def test_attend_ext_struct_matches_header():
+    """The binding's polykv_attend_ext mirrors include/polykv.h field by field."""
+    import ctypes
+    import serving_q8_encode_gb300 as pk
+    names = [f[0] for f in pk.AttendExt._fields_]
+    hdr = open(os.path.join(ROOT, "include", "polykv.h")).read()
+    body = hdr[hdr.index("typedef struct {\n    /* Private per-agent suffix"):hdr.index("} polykv_attend_ext;")]
+    import re
+    declared = re.findall(r"^\s+(?:const void\*|int64_t)\s+(\w+);", body, re.M)
+    assert names == declared
+    assert ctypes.sizeof(pk.AttendExt) == 48

@@ -246,3 +246,52 @@ def test_suffix_smollm2_mha_fp16(env, path):
 
 def test_suffix_peaky(env, path):
     run_suffix_case(env, 1, 2, 8, 128, 500, 2, 128, "bf16", q_mult=8.0)
+
+
+# ---- query-chunk mode: C query tokens per agent, each with its own key/value, causal inside the chunk
+def run_chunk_case(env, L, H, Hq, d, T, A, C, dtype, seed=0, q_mult=1.0):
+    pk, torch, c32, b32 = env
+    kb, vb = synth.gen_kv(L, H, T, d, dtype, seed)
+    qb = synth.gen_q(L, A * C, Hq, d, dtype, seed, q_mult=q_mult).reshape(L, A, C, Hq, d)
+    ck, cv = synth.gen_suffix(L, A, H, C, d, dtype, seed)   # [L][A][H][C][d]
+    pool = pk.Pool(L, H, d, T, dtype)
+    pool.encode(_dev(torch, kb), _dev(torch, vb))
+    out = pool.attend_chunk(_dev(torch, qb), T, _dev(torch, ck), _dev(torch, cv))
+    torch.cuda.synchronize()
+    assert pool.status() == 0
+    ref_pool = oracle.attention.encode_pool(kb, vb, dtype, b32)
+    ref = oracle.attention.attend_pool(qb, dtype, ref_pool, T, c32, chunk_k_bits=ck, chunk_v_bits=cv)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() <= ATOL, f"max abs err {err.max():.3e}"
+
+
+def test_chunk_64_tokens_llama3_8b_shape(env, path):
+    run_chunk_case(env, 1, 8, 32, 128, 1024, 2, 64, "bf16")
+
+
+@pytest.mark.parametrize("C", [1, 2, 33, 65, 130])
+def test_chunk_ragged_lengths(env, path, C):
+    run_chunk_case(env, 1, 2, 8, 128, 300, 2, C, "bf16", seed=C)
+
+
+def test_chunk_smollm2_mha_fp16(env, path):
+    run_chunk_case(env, 1, 32, 32, 64, 600, 1, 16, "f16")
+
+
+def test_chunk_peaky(env, path):
+    run_chunk_case(env, 1, 2, 8, 128, 500, 2, 32, "bf16", q_mult=8.0)
+
+
+def test_chunk_of_one_equals_one_token_suffix(env):
+    """A chunk of length 1 is a one-token private suffix (same keys/values, same softmax)."""
+    pk, torch, c32, b32 = env
+    L, H, Hq, d, T, A = 1, 2, 8, 128, 200, 3
+    kb, vb = synth.gen_kv(L, H, T, d, "bf16", 5)
+    qb = synth.gen_q(L, A, Hq, d, "bf16", 5)
+    sk, sv = synth.gen_suffix(L, A, H, 1, d, "bf16", 5)
+    pool = pk.Pool(L, H, d, T, "bf16")
+    pool.encode(_dev(torch, kb), _dev(torch, vb))
+    a = pool.attend_with_suffix(_dev(torch, qb), T, _dev(torch, sk), _dev(torch, sv))
+    b = pool.attend_chunk(_dev(torch, qb).view(L, A, 1, Hq, d), T, _dev(torch, sk), _dev(torch, sv))
+    torch.cuda.synchronize()
+    assert (a - b.view(L, A, Hq, d)).abs().max().item() <= 1e-5

@@ -413,3 +413,21 @@ def test_q8_subnormal_scale_clamp_binds():
     q, s = keys.quantize_q8_0(x)
     assert float(s[0, 0]) == 2.0 ** -24
     assert q[0, 0] == 127 and q[0, 1] == -127 and q[0, 2] == 50
+
+
+def test_attend_pool_chunk_layout_matches_suffix_per_position():
+    """attend_pool in chunk mode ([L][A][H][C][d] chunk K/V, q [L][A][C][Hq][d]) equals, for every
+    chunk position c, a suffix of the first c+1 chunk tokens (the suffix path is a separate function)."""
+    import synth
+    c32, b32 = codebook.codebook_f32()
+    L, H, Hq, d, T, A, C = 1, 2, 4, 64, 40, 2, 5
+    kb, vb = synth.gen_kv(L, H, T, d, "f16", 3)
+    pool = attention.encode_pool(kb, vb, "f16", b32)
+    qb = synth.gen_q(L, A * C, Hq, d, "f16", 3).reshape(L, A, C, Hq, d)
+    ck, cv = synth.gen_suffix(L, A, H, C, d, "f16", 3)
+    got = attention.attend_pool(qb, "f16", pool, T, c32, chunk_k_bits=ck, chunk_v_bits=cv)
+    for c in range(C):
+        ref = attention.attend_pool(np.ascontiguousarray(qb[:, :, c]), "f16", pool, T, c32,
+                                    suffix_k_bits=np.ascontiguousarray(ck[:, :, :, :c + 1]),
+                                    suffix_v_bits=np.ascontiguousarray(cv[:, :, :, :c + 1]))
+        assert np.allclose(got[:, :, c], ref, atol=1e-12, rtol=0)
