@@ -50,6 +50,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_bf16_tflops():
+    """Dense bf16 tensor peak (TFLOP/s, burst) from MEASURED_PEAKS.json, else the fallback figure."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f).get("bf16_tflops", 1900.0))
+    return 1900.0
+
+
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -358,6 +367,7 @@ def run_sweep(args):
     L, H, Hq, d = base.n_layers, base.n_kv_heads, base.n_q_heads, base.head_dim
     dev = torch.device("cuda", 0)
     peak, peak_src = measured_peaks()
+    bf16_peak = measured_bf16_tflops()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -398,10 +408,39 @@ def run_sweep(args):
             rows.append({"mode": "attend", "n_ctx": T, "n_agents": A, "us": att_us,
                          "gbs": att_b / (att_us * 1e-6) / 1e9, "frac_of_peak": att_b / (att_us * 1e-6) / 1e9 / peak,
                          "pool_bytes": att_b - L * A * Hq * d * 6})
+            del out, ws
+            if args.chunk > 0:
+                # query-chunk mode: C query tokens per agent with their own K/V, causal inside the chunk;
+                # the pool part is a dense contraction (R = A*C*G rows per kv head), so report tensor use
+                C = args.chunk
+                qcb = synth.gen_q(L, A * C, Hq, d, base.dtype, seed=1).reshape(L, A, C, Hq, d)
+                ckb, cvb = synth.gen_suffix(L, A, H, C, d, base.dtype, seed=1)
+                qc = torch.from_numpy(qcb.view(np.int16)).to(dev)
+                ck = torch.from_numpy(ckb.view(np.int16)).to(dev)
+                cv = torch.from_numpy(cvb.view(np.int16)).to(dev)
+                del qcb, ckb, cvb
+                outc = torch.empty((L, A, C, Hq, d), dtype=torch.float32, device=dev)
+                ext = pk.AttendExt(chunk_k=ck.data_ptr(), chunk_v=cv.data_ptr(), chunk_len=C)
+                wsc = torch.empty(max(16, pk.polykv_attend_ex_workspace_size(pool.handle, A, Hq, T, ext)),
+                                  dtype=torch.uint8, device=dev)
+                ch_us = timed(lambda: pool.attend_chunk(qc, T, ck, cv, out=outc, workspace=wsc, stream=stream),
+                              max(2, args.steps // 4))
+                R = A * C * (Hq // H)
+                flops = 4.0 * R * T * d * L * H + 4.0 * (C * (C + 1) / 2) * (Hq // H) * d * L * A * H
+                # tensor-core MMAs issued: keys twice (exact hi/lo halves), values once; rows padded to 64
+                mma_flops = 2.0 * 128 * 64 * 16 * (16 + 8) * ((R + 63) // 64) * ((T + 127) // 128) * L * H
+                rows.append({"mode": "attend_chunk", "n_ctx": T, "n_agents": A, "chunk": C, "us": ch_us,
+                             "query_tokens_per_s": A * C / (ch_us * 1e-6),
+                             "tflops": flops / (ch_us * 1e-6) / 1e12,
+                             "tensor_issued_tflops": mma_flops / (ch_us * 1e-6) / 1e12,
+                             "tensor_frac_of_bf16_peak": mma_flops / (ch_us * 1e-6) / 1e12 / bf16_peak})
+                del qc, ck, cv, outc, wsc
+                torch.cuda.empty_cache()
         del pool, k, v
         torch.cuda.empty_cache()
     print(json.dumps({"sweep": "llama3_8b shape, encode-only and attend-only", "peak_gbs": peak,
-                      "peak_source": peak_src, "l2": "flushed before each launch", "rows": rows}), flush=True)
+                      "peak_source": peak_src, "bf16_tflops_peak": bf16_peak, "l2": "flushed before each launch",
+                      "rows": rows}), flush=True)
     return 0
 
 
@@ -416,6 +455,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--sweep", action="store_true",
                     help="encode-only / attend-only grid over context {600,1851,4096,7194} x agents {1,2,4,8,15}")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="with --sweep: also time query-chunk mode with this many query tokens per agent")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (smaller cases for profiler captures)")
     args = ap.parse_args()

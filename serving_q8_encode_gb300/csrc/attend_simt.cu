@@ -273,34 +273,39 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
 template <int D>
 __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
                                                     float* __restrict__ out, int U, int H, int A, int Hq, int R,
-                                                    int n_slots, int64_t nt, int64_t tt, int nc,
+                                                    int n_slots, MergeLayout lay,
                                                     const float* __restrict__ sfx_acc,
                                                     const float* __restrict__ sfx_ml) {
     constexpr int EPL = D / 32;  // elements per lane
     const int wid = blockIdx.x * 4 + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if (wid >= U * R) return;
+    if ((int64_t)wid >= (int64_t)U * R) return;
     const int unit = wid / R, r = wid % R;
     const int G = Hq / H;
     const int layer = unit / H, kvh = unit % H;
     const int a = r / G, g = r % G;
 
+    // partial rows of this output row: pr(s) = first + s * stride, s < pieces
     int pieces = n_slots;
-    if (nc > 0) {
-        const int64_t lo = (((int64_t)unit * nt + 1) * nc - 1) / tt;
-        const int64_t hi = (((int64_t)unit * nt + nt) * nc - 1) / tt;
+    int64_t first = (int64_t)unit * n_slots * R + r, stride = R;
+    if (lay.nc > 0) {
+        const int64_t seg = (int64_t)unit * lay.nrg + r / lay.RS;
+        const int64_t lo = ((seg * lay.nt + 1) * lay.nc - 1) / lay.tt;
+        const int64_t hi = ((seg * lay.nt + lay.nt) * lay.nc - 1) / lay.tt;
         pieces = (int)(hi - lo + 1);
+        first = (seg + lo) * lay.RS + r % lay.RS;
+        stride = lay.RS;
     }
     const int64_t orow = ((int64_t)layer * A + a) * Hq + kvh * G + g;   // output / suffix row
     float M = -INFINITY;
-    for (int s = 0; s < pieces; ++s) M = fmaxf(M, ws_ml[(((int64_t)unit * n_slots + s) * R + r) * 2]);
+    for (int s = 0; s < pieces; ++s) M = fmaxf(M, ws_ml[(first + s * stride) * 2]);
     if (sfx_ml) M = fmaxf(M, sfx_ml[orow * 2]);
     float L = 0.0f;
     float o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
     for (int s = 0; s < pieces; ++s) {
-        const int64_t pr = ((int64_t)unit * n_slots + s) * R + r;
+        const int64_t pr = first + s * stride;
         const float ms = ws_ml[pr * 2];
         if (ms == -INFINITY) continue;
         const float w = exp2f(ms - M);
@@ -367,7 +372,7 @@ polykv_status run_simt(const PoolView& p, const void* q, float* out, int A, int 
         const polykv_status ss = launch_attend_suffix(*sfx, BF16 ? POLYKV_BF16 : POLYKV_F16, p.L, A, p.H, Hq, D, scale, st);
         if (ss != POLYKV_OK) return ss;
     }
-    return launch_attend_merge(ws_acc, ws_ml, out, U, p.H, A, Hq, R, n_splits, 0, 0, 0, D, st,
+    return launch_attend_merge(ws_acc, ws_ml, out, U, p.H, A, Hq, R, n_splits, MergeLayout(), D, st,
                                sfx ? sfx->acc : nullptr, sfx ? sfx->ml : nullptr);
 }
 
@@ -395,16 +400,14 @@ int64_t split_length(const PoolView& p, int rows, int64_t n_ctx) {
 }  // namespace
 
 polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float* out, int U, int H, int A, int Hq,
-                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st,
+                                  int R, int n_slots, const MergeLayout& lay, int D, cudaStream_t st,
                                   const float* sfx_acc, const float* sfx_ml) {
     const int64_t warps = (int64_t)U * R;
     const unsigned blocks = (unsigned)((warps + 3) / 4);
     if (D == 128)
-        attend_merge<128><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc, sfx_acc,
-                                                  sfx_ml);
+        attend_merge<128><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
     else
-        attend_merge<64><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, nt, tt, nc, sfx_acc,
-                                                 sfx_ml);
+        attend_merge<64><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend merge launch: %s", cudaGetErrorString(e));
     return POLYKV_OK;

@@ -95,10 +95,12 @@ struct TcParams {
     float* ws_ml;
     int64_t n_ctx;
     int64_t total_tiles;
-    int A, Hq, G, R;
-    int nt;      // tiles per unit
+    int A, Hq, G;
+    int Rtot;    // query rows per kv head (agents x GQA group)
+    int nrg;     // groups of up to 64 rows per kv head; a segment is one (kv-head unit, row group)
+    int RS;      // rows per partial slot (64 with several row groups, else Rtot)
+    int nt;      // tiles per segment (= per unit)
     int nctas;
-    int pmax;    // partial slots per unit
     int test_stall;  // test hook: the MMA thread issues nothing, so the softmax waits run out
     float scale_log2;
 };
@@ -287,8 +289,8 @@ __device__ __forceinline__ float unit_wscale(float nmax) {
 // of two into the MMA1 operand, the logit scale and the value scale w.
 template <bool QBF16>
 __device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, const float* __restrict__ nmax, int64_t u,
-                                              int H, int A, int Hq, int G, int R, float scale_log2, uint8_t* sQ,
-                                              Misc& M, int si, int wi, int lane) {
+                                              int r0, int H, int A, int Hq, int G, int R, float scale_log2,
+                                              uint8_t* sQ, Misc& M, int si, int wi, int lane) {
     const int layer = (int)(u / H), kvh = (int)(u % H);
     uint4 qv[4];
     float qm = 0.0f;
@@ -298,7 +300,7 @@ __device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, co
         qv[m] = make_uint4(0u, 0u, 0u, 0u);
         if (cid < R * 16) {
             const int r = cid >> 4, dc = cid & 15;
-            const int a = r / G, gq = r % G;
+            const int a = (r0 + r) / G, gq = (r0 + r) % G;
             qv[m] = __ldg(reinterpret_cast<const uint4*>(
                               q + (((int64_t)layer * A + a) * Hq + kvh * G + gq) * kD) + dc);
             const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
@@ -365,8 +367,9 @@ __device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, co
 // Segment epilogue (one row group): row sums over the token slots, then the rows' O^T columns
 // (divided by w) and (m, l) written as the partial for (unit, piece) `slot`.
 __device__ __noinline__ void softmax_epilogue(Misc& M, int s, uint32_t ph, volatile int* abortp, uint32_t lane_addr,
-                                              int grp, int wq, int lane, int tt, int rbase, int R, uint32_t gbar,
-                                              int64_t slot, float* __restrict__ ws_acc, float* __restrict__ ws_ml) {
+                                              int grp, int wq, int lane, int tt, int rbase, int R, int RS,
+                                              uint32_t gbar, int64_t slot, float* __restrict__ ws_acc,
+                                              float* __restrict__ ws_ml) {
     tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph, abortp, kTimeoutNs);
     tc::fence_after();
     tc::wait_st();
@@ -393,13 +396,13 @@ __device__ __noinline__ void softmax_epilogue(Misc& M, int s, uint32_t ph, volat
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const int r = rbase + 16 * cc + k;
-            if (r < R) ws_acc[(slot * R + r) * kD + tt] = __uint_as_float(to[k]) * unscale;
+            if (r < R) ws_acc[(slot * RS + r) * kD + tt] = __uint_as_float(to[k]) * unscale;
         }
     }
     if (tt < 32 && rbase + tt < R) {
         const int r = rbase + tt;
-        ws_ml[(slot * R + r) * 2] = M.m[r];
-        ws_ml[(slot * R + r) * 2 + 1] =
+        ws_ml[(slot * RS + r) * 2] = M.m[r];
+        ws_ml[(slot * RS + r) * 2 + 1] =
             M.red[grp][0][tt] + M.red[grp][1][tt] + M.red[grp][2][tt] + M.red[grp][3][tt];
     }
     tc::fence_before();
@@ -466,8 +469,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // =============================== TMA: scales / value codes / norms into the ring
         if (lane == 0) {
             int issued = 0;
-            int64_t u = g0 / nt;
-            int ti = (int)(g0 - u * nt);
+            int64_t sg = g0 / nt;                  // segment
+            int64_t u = sg / P.nrg;                // its pool unit
+            int ti = (int)(g0 - sg * nt);
             for (int j = 0; j < n && !*abortp; ++j) {
                 const int st = j & (kNS - 1);
                 if (j >= kNS &&
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 const int64_t row0 = u * cap + (int64_t)ti * kTile;
                 if (++ti == nt) {
                     ti = 0;
-                    ++u;
+                    u = ++sg / P.nrg;
                 }
                 const uint32_t dst = tc::smem_u32(sR + st * kRawStage);
                 const uint32_t bar = tc::smem_u32(&M.rfull[st]);
@@ -502,34 +506,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t lane_addr = tbase + ((q4 * 32u) << 16);
         const uint32_t t = q4 * 32u + (uint32_t)lane;
         const uint32_t krow = tc::smem_u32(sK) + t * kKRow + (uint32_t)(2 * pg) * kKStage;
-        auto adv2 = [&](int64_t& uu, int& tix) {
+        auto adv2 = [&](int64_t& sg, int& tix) {   // two tiles on, across segments
             tix += 2;
             while (tix >= nt) {
                 tix -= nt;
-                ++uu;
+                ++sg;
             }
         };
-        int64_t u_n = (g0 + pg) / nt;
+        int64_t u_n = (g0 + pg) / nt;              // segment of the next key-row copy
         int ti_n = (int)((g0 + pg) - u_n * nt);
+        int64_t pu_n = u_n / P.nrg;                // its pool unit and row group, advanced incrementally
+        int rg_n = (int)(u_n - pu_n * P.nrg);
         int kk = 0;
         // copy the key row of this token slot for this group's tile jj into the group's stage kk & 1
         auto issue_k = [&](int jj) {
             if (jj < n) {
                 const int64_t tok = (int64_t)ti_n * kTile + t;
                 const bool ok = tok < P.n_ctx;
-                const int8_t* src = P.p.kq + (u_n * cap + (ok ? tok : 0)) * kD;
+                const int8_t* src = P.p.kq + (pu_n * cap + (ok ? tok : 0)) * kD;
                 const uint32_t dst = krow + (uint32_t)(kk & 1) * kKStage;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) cp_async16(dst + 16u * i, src + 16 * i, ok ? 16u : 0u);
-                adv2(u_n, ti_n);
+                ti_n += 2;
+                while (ti_n >= nt) {
+                    ti_n -= nt;
+                    if (++rg_n == P.nrg) {
+                        rg_n = 0;
+                        ++pu_n;
+                    }
+                }
             }
             ++kk;
             cp_async_commit();
         };
         issue_k(pg);
-        int64_t u = (g0 + pg) / nt;
+        int64_t u = (g0 + pg) / nt;                // segment of the current tile
         int ti = (int)((g0 + pg) - u * nt);
-        float wscale = pg < n ? unit_wscale(P.p.nmax[u]) : 1.0f;
+        float wscale = pg < n ? unit_wscale(P.p.nmax[u / P.nrg]) : 1.0f;
         const int s = pg;
         int k = 0;
         // The loop always runs to its end so that all 128 threads of the group meet at the same
@@ -604,7 +617,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::mbar_arrive(tc::smem_u32(&M.vfull[s]));
             const int64_t u_prev = u;
             adv2(u, ti);
-            if (u != u_prev && j + 2 < n) wscale = unit_wscale(P.p.nmax[u]);
+            if (u != u_prev && j + 2 < n) wscale = unit_wscale(P.p.nmax[u / P.nrg]);
         }
         cp_async_wait<0>();   // no copy may land in shared memory after the CTA exits
     } else if (warp < 16) {
@@ -615,7 +628,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int si = tid - 256;               // 0..255 over both groups
         const uint32_t lane_addr = tbase + ((uint32_t)(wq * 32) << 16);
         const uint32_t gbar = 1 + grp;
-        const int R = P.R;
+        int R = 0;                               // rows of the current segment
         const int rbase = 32 * grp;
         int seg = -1;
         int64_t seg_u = -1;
@@ -633,8 +646,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (first) {
                 ++seg;
                 seg_u = u;
-                softmax_prologue<QBF16>(P.q, P.p.nmax, u, P.p.H, P.A, P.Hq, P.G, P.R, P.scale_log2, sQ, M, si, warp - 8,
-                                        lane);
+                const int rg = (int)(u % P.nrg);
+                R = min(kNR, P.Rtot - kNR * rg);
+                softmax_prologue<QBF16>(P.q, P.p.nmax, u / P.nrg, kNR * rg, P.p.H, P.A, P.Hq, P.G, R, P.scale_log2, sQ,
+                                        M, si, warp - 8, lane);
             }
             const float scale_eff = M.scale_eff;
             const bool tail = (int64_t)(ti + 1) * kTile > P.n_ctx;
@@ -726,9 +741,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::mbar_arrive(tc::smem_u32(&M.pfull[s]));
 
             if (last) {
-                const int64_t ulo = cta_of_tile(seg_u * nt, TT, P.nctas);
-                softmax_epilogue(M, s, ph, abortp, lane_addr, grp, wq, lane, tt, rbase, R, gbar,
-                                 seg_u * P.pmax + (c - ulo), P.ws_acc, P.ws_ml);
+                // one partial per (segment, CTA): slot = segment + CTA (distinct, at most segments + CTAs)
+                softmax_epilogue(M, s, ph, abortp, lane_addr, grp, wq, lane, tt, rbase, R, P.RS, gbar, seg_u + c,
+                                 P.ws_acc, P.ws_ml);
             }
         }
     } else if (warp == 16 && lane == 0) {
@@ -826,35 +841,31 @@ int num_sms() {
 }
 
 struct TcPlan {
-    int64_t nt, tt;
-    int nctas, pmax;
+    int64_t nt, tt, nseg;
+    int nctas, nrg, RS;
+    size_t slots;   // one partial per (segment, CTA that works on it): slot = segment + CTA
 };
 
-TcPlan plan(const PoolView& p, int64_t n_ctx) {
+TcPlan plan(const PoolView& p, int rows, int64_t n_ctx) {
     TcPlan pl;
     pl.nt = (n_ctx + kTile - 1) / kTile;
-    const int64_t U = (int64_t)p.L * p.H;
-    pl.tt = U * pl.nt;
+    pl.nrg = (rows + kNR - 1) / kNR;
+    pl.RS = pl.nrg > 1 ? kNR : rows;
+    pl.nseg = (int64_t)p.L * p.H * pl.nrg;
+    pl.tt = pl.nseg * pl.nt;
     const int64_t sms = num_sms();
     pl.nctas = (int)(pl.tt < sms ? pl.tt : sms);
-    int pm = 1;
-    for (int64_t u = 0; u < U; ++u) {
-        const int64_t lo = ((u * pl.nt + 1) * pl.nctas - 1) / pl.tt;
-        const int64_t hi = (((u + 1) * pl.nt) * pl.nctas - 1) / pl.tt;
-        if (hi - lo + 1 > pm) pm = (int)(hi - lo + 1);
-    }
-    pl.pmax = pm;
+    pl.slots = (size_t)(pl.nseg + pl.nctas);
     return pl;
 }
 
 }  // namespace
 
-bool attend_tc_supported(const PoolView& p, int rows) { return p.d == kD && rows >= 1 && rows <= kNR; }
+bool attend_tc_supported(const PoolView& p, int rows) { return p.d == kD && rows >= 1; }
 
 size_t attend_tc_workspace(const PoolView& p, int rows, int64_t n_ctx) {
-    const TcPlan pl = plan(p, n_ctx);
-    const size_t U = (size_t)p.L * p.H;
-    return sizeof(float) * U * (size_t)pl.pmax * (size_t)rows * (size_t)(kD + 2);
+    const TcPlan pl = plan(p, rows, n_ctx);
+    return sizeof(float) * pl.slots * (size_t)pl.RS * (size_t)(kD + 2);
 }
 
 polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
@@ -863,24 +874,24 @@ polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q
     const int G = n_q_heads / p.H;
     const int R = n_agents * G;
     if (!attend_tc_supported(p, R)) return set_error(POLYKV_E_UNSUPPORTED, "tensor-core attend: d=%d rows=%d", p.d, R);
-    const TcPlan pl = plan(p, n_ctx);
+    const TcPlan pl = plan(p, R, n_ctx);
     const size_t need = attend_tc_workspace(p, R, n_ctx);
     if (ws_bytes < need) return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend: workspace %zu < %zu bytes", ws_bytes, need);
-    const size_t U = (size_t)p.L * p.H;
     TcParams P;
     P.p = p;
     P.q = static_cast<const uint16_t*>(q);
     P.ws_acc = static_cast<float*>(ws);
-    P.ws_ml = P.ws_acc + U * (size_t)pl.pmax * (size_t)R * kD;
+    P.ws_ml = P.ws_acc + pl.slots * (size_t)pl.RS * kD;
     P.n_ctx = n_ctx;
     P.total_tiles = pl.tt;
     P.A = n_agents;
     P.Hq = n_q_heads;
     P.G = G;
-    P.R = R;
+    P.Rtot = R;
+    P.nrg = pl.nrg;
+    P.RS = pl.RS;
     P.nt = (int)pl.nt;
     P.nctas = pl.nctas;
-    P.pmax = pl.pmax;
     P.scale_log2 = scale * kLog2eTc;
     // Test hook for the bounded-wait path: POLYKV_TEST_STALL=1 makes every wait on the tensor-core
     // results run out; the CTA then gives up, releases its TMEM and sets the pool's status word.
@@ -896,8 +907,14 @@ polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q
         const polykv_status ss = launch_attend_suffix(*sfx, dt, p.L, n_agents, p.H, n_q_heads, kD, scale, stream);
         if (ss != POLYKV_OK) return ss;
     }
-    return launch_attend_merge(P.ws_acc, P.ws_ml, out, (int)U, p.H, n_agents, n_q_heads, R, pl.pmax, pl.nt, pl.tt,
-                               pl.nctas, kD, stream, sfx ? sfx->acc : nullptr, sfx ? sfx->ml : nullptr);
+    MergeLayout ml;
+    ml.nrg = pl.nrg;
+    ml.RS = pl.RS;
+    ml.nt = pl.nt;
+    ml.tt = pl.tt;
+    ml.nc = pl.nctas;
+    return launch_attend_merge(P.ws_acc, P.ws_ml, out, p.L * p.H, p.H, n_agents, n_q_heads, R, 0, ml, kD, stream,
+                               sfx ? sfx->acc : nullptr, sfx ? sfx->ml : nullptr);
 }
 
 }  // namespace polykv

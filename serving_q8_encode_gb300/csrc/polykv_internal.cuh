@@ -62,8 +62,16 @@ polykv_status launch_attend_simt(const PoolView& p, polykv_dtype dt, const void*
                                  int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
                                  cudaStream_t stream, const SuffixArgs* sfx = nullptr);
 
+// Where the pool partials are. nc == 0: CUDA-core splits, slot = unit * n_slots + split, R rows
+// per slot. nc > 0: the tensor-core partition of (segment = unit x row group, tile) over nc CTAs,
+// slot = segment + CTA, RS rows per slot, nrg row groups of 64 rows per unit.
+struct MergeLayout {
+    int nrg = 1, RS = 0;
+    int64_t nt = 0, tt = 0;
+    int nc = 0;
+};
 polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float* out, int U, int H, int A, int Hq,
-                                  int R, int n_slots, int64_t nt, int64_t tt, int nc, int D, cudaStream_t st,
+                                  int R, int n_slots, const MergeLayout& ml, int D, cudaStream_t st,
                                   const float* sfx_acc = nullptr, const float* sfx_ml = nullptr);
 
 // tensor-core attention path (head_dim 128, up to 64 rows per kv head)
