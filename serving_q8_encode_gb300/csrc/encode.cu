@@ -93,23 +93,34 @@ __device__ __forceinline__ void unpack32(const uint4 (&raw)[4], float (&x)[32], 
     }
 }
 
-__device__ __forceinline__ uint32_t ge_mask_s32(int32_t a, int32_t b) {
+__device__ __forceinline__ uint32_t ge_mask_f32(float a, float b) {
     uint32_t m;  // 0xFFFFFFFF if a >= b else 0
-    asm("set.ge.u32.s32 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
     return m;
 }
 
-// code = number of boundaries b_i * ||v|| <= y, on the float bits: the boundaries are symmetric
-// (b_{6-i} = -b_i, b_3 = 0), non-negative floats order like their bit patterns, and for y < 0
-// "y >= -t" is "|y| <= t", i.e. not "|y| > t" -- taking one off |y|'s bits turns the strict
-// comparison into >=. y = -0 counts as non-negative (the boundary 0 is <= -0).
-__device__ __forceinline__ uint32_t value_code_thr(float y, int32_t t4, int32_t t5, int32_t t6) {
-    const int32_t bits = __float_as_int(y);
-    int32_t sm;                                      // -1 for y < 0 (not -0), else 0
-    asm("set.lt.s32.f32 %0, %1, 0f00000000;" : "=r"(sm) : "f"(y));
-    const int32_t t = (bits & 0x7FFFFFFF) + sm;
-    const uint32_t neg_count = ge_mask_s32(t, t4) + ge_mask_s32(t, t5) + ge_mask_s32(t, t6);  // minus the count
-    return (4u - neg_count) ^ ((uint32_t)sm & 7u);
+// code = number of boundaries b_i * ||v|| <= y. The boundaries are symmetric (b_{6-i} = -b_i,
+// b_3 = 0): with m = #{i in 4..6 : |y| >= t_i}, the code is 4 + m for y >= 0 (y = -0 included) and
+// 3 - m = (4 + m) ^ 7 for y < 0. For y < 0 the definition compares |y| > t_i; using >= there
+// differs only when |y| equals a scaled boundary, inside the boundary exemption.
+__device__ __forceinline__ uint32_t value_code_thr(float y, float t4, float t5, float t6) {
+    uint32_t sm;                                      // 0xFFFFFFFF for y < 0 (not -0), else 0
+    asm("set.lt.u32.f32 %0, %1, 0f00000000;" : "=r"(sm) : "f"(y));
+    const float ay = fabsf(y);
+    const uint32_t neg_m = ge_mask_f32(ay, t4) + ge_mask_f32(ay, t5) + ge_mask_f32(ay, t6);   // minus m
+    return (4u - neg_m) ^ (sm & 7u);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// trunc(r + copysign(0.5 + 2^-14, r)) with the addition rounded toward zero = sign(r) * floor(|r| + 0.5 + 2^-14)
+__device__ __forceinline__ int round_away(float r) {
+    const float c = __uint_as_float((__float_as_uint(r) & 0x80000000u) | 0x3F000400u);   // +-(0.5 + 2^-14)
+    return __float2int_rz(__fadd_rz(r, c));
 }
 
 __device__ __forceinline__ uint32_t bytes4(int a, int b, int c, int d) {
@@ -122,17 +133,16 @@ __device__ __forceinline__ uint32_t bytes4(int a, int b, int c, int d) {
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+__global__ void __launch_bounds__(256, 4) encode_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                                                      PoolView p, int64_t n_tok, int64_t t0, int64_t n_vec) {
     constexpr int LPV = D / 32;          // lanes per vector
     constexpr int VPB = 256 / LPV;       // vectors per block
-    __shared__ float s_norm[VPB];
     const int gl = threadIdx.x % LPV;
     const int vloc = threadIdx.x / LPV;
     const int64_t vi_raw = (int64_t)blockIdx.x * VPB + vloc;
     const bool valid = vi_raw < n_vec;
     const int64_t vi = valid ? vi_raw : n_vec - 1;   // every lane takes part in the shuffles
-    const int64_t unit = vi / n_tok;
+    const int64_t unit = n_vec <= 0xFFFFFFFFll ? (int64_t)((uint32_t)vi / (uint32_t)n_tok) : vi / n_tok;
     const int64_t pidx = unit * p.cap + t0 + (vi - unit * n_tok);
 
     // both 64-byte rows are requested before any arithmetic (one memory round trip per lane)
@@ -146,7 +156,7 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
         unpack32(kraw, x, BF16);
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        for (int i = 0; i < 32; i += 2) amax = max3(amax, fabsf(x[i]), fabsf(x[i + 1]));
         const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
         const float sf = __half2float(s16);
         // a block whose scale is 0 or not finite gets zero codes (y = 0 makes every x * y zero)
@@ -154,15 +164,22 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
         const float yb = usable ? __frcp_rn(sf) : 0.0f;
         const float2 yb2 = make_float2(yb, yb);
         uint32_t packed[8];
-        int cq[4];
+        // round half away from zero: trunc(RN(x * y) +- (0.5 + 2^-14)) with the addition rounded
+        // toward zero; with a normal scale |x / s16| <= 127.06, so no clamp is needed, while a
+        // subnormal scale can take it up to ~189 and the code is clamped to [-127, 127]
+        const bool clamp = !(sf >= 6.103515625e-05f);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            const float2 r = mul2(make_float2(x[i], x[i + 1]), yb2);
-            const int a0 = min(127, (int)__fadd_rz(fabsf(r.x), 0.50006103515625f));   // 0.5 + 2^-14
-            const int a1 = min(127, (int)__fadd_rz(fabsf(r.y), 0.50006103515625f));
-            cq[i & 3] = r.x < 0.0f ? -a0 : a0;
-            cq[(i & 3) + 1] = r.y < 0.0f ? -a1 : a1;
-            if ((i & 3) == 2) packed[i >> 2] = bytes4(cq[0], cq[1], cq[2], cq[3]);
+        for (int i = 0; i < 32; i += 4) {
+            const float2 r01 = mul2(make_float2(x[i], x[i + 1]), yb2);
+            const float2 r23 = mul2(make_float2(x[i + 2], x[i + 3]), yb2);
+            int q0 = round_away(r01.x), q1 = round_away(r01.y), q2 = round_away(r23.x), q3 = round_away(r23.y);
+            if (clamp) {
+                q0 = max(-127, min(127, q0));
+                q1 = max(-127, min(127, q1));
+                q2 = max(-127, min(127, q2));
+                q3 = max(-127, min(127, q3));
+            }
+            packed[i >> 2] = bytes4(q0, q1, q2, q3);
         }
         if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.kq + pidx * D + gl * 32);
@@ -232,9 +249,9 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
         }
     }
     // boundaries scaled by the norm (positive ones; the negative ones mirror them)
-    const int32_t t4 = __float_as_int(__fmul_rn(kB4, nrm));
-    const int32_t t5 = __float_as_int(__fmul_rn(kB5, nrm));
-    const int32_t t6 = __float_as_int(__fmul_rn(kB6, nrm));
+    const float t4 = __fmul_rn(kB4, nrm);
+    const float t5 = __fmul_rn(kB5, nrm);
+    const float t6 = __fmul_rn(kB6, nrm);
     const bool nz = nrm > 0.0f;
     uint32_t w24[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
@@ -251,22 +268,16 @@ __global__ void __launch_bounds__(256) encode_kernel(const uint16_t* __restrict_
         dst[2] = (w24[2] >> 16) | (w24[3] << 8);
         if (gl == 0) p.vn[pidx] = __float2half_rn(nrm);
     }
-    // running per-unit maximum of ||v|| (an upper bound used by attention to scale fp16 operands)
-    if (gl == 0) s_norm[vloc] = valid ? nrm : 0.0f;
-    __syncthreads();
-    if (threadIdx.x < VPB) {
-        const int64_t my = (int64_t)blockIdx.x * VPB + threadIdx.x;
-        const int64_t blk_end = (int64_t)blockIdx.x * VPB + VPB;
-        const int64_t last = (blk_end < n_vec ? blk_end : n_vec) - 1;
-        if (my <= last) {
-            const int64_t u_my = my / n_tok;
-            const bool head = threadIdx.x == 0 || ((my - 1) / n_tok) != u_my;
-            if (head) {
-                float mx = 0.0f;
-                for (int64_t w = my; w <= last && w / n_tok == u_my; ++w) mx = fmaxf(mx, s_norm[w - (int64_t)blockIdx.x * VPB]);
-                atomicMax(reinterpret_cast<unsigned int*>(p.nmax) + u_my, __float_as_uint(mx));
-            }
-        }
+    // running per-unit maximum of ||v|| (an upper bound used by attention to scale fp16 operands):
+    // one max-reduction per warp and one atomic when the warp's vectors share a unit (the common
+    // case), else one atomic per vector. Norms are non-negative, so their bit patterns order as uints.
+    const uint32_t nb = (gl == 0 && valid) ? __float_as_uint(nrm) : 0u;
+    const int64_t unit0 = __shfl_sync(0xffffffffu, unit, 0);
+    if (__all_sync(0xffffffffu, unit == unit0)) {
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, nb);
+        if ((threadIdx.x & 31) == 0 && mx != 0u) atomicMax(reinterpret_cast<unsigned int*>(p.nmax) + unit0, mx);
+    } else if (gl == 0 && valid && nb != 0u) {
+        atomicMax(reinterpret_cast<unsigned int*>(p.nmax) + unit, nb);
     }
 }
 
