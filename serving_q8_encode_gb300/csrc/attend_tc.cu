@@ -650,6 +650,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 R = min(kNR, P.Rtot - kNR * rg);
                 softmax_prologue<QBF16>(P.q, P.p.nmax, u / P.nrg, kNR * rg, P.p.H, P.A, P.Hq, P.G, R, P.scale_log2, sQ,
                                         M, si, warp - 8, lane);
+                // the next segment's query rows go to L2 now, so its prologue does not wait on HBM
+                const int64_t un = u + 1;
+                if (un < (g1 + nt - 1) / nt && si < kNR * 2) {
+                    const int rgn = (int)(un % P.nrg);
+                    const int rn = kNR * rgn + (si >> 1);          // two threads per row, 128 B each
+                    if (rn < P.Rtot && (si >> 1) < kNR) {
+                        const int64_t pun = un / P.nrg;
+                        const int layer = (int)(pun / P.p.H), kvh = (int)(pun % P.p.H);
+                        const uint16_t* qa = P.q + (((int64_t)layer * P.A + rn / P.G) * P.Hq + kvh * P.G + rn % P.G) * kD +
+                                             (si & 1) * 64;
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(qa));
+                    }
+                }
             }
             const float scale_eff = M.scale_eff;
             const bool tail = (int64_t)(ti + 1) * kTile > P.n_ctx;

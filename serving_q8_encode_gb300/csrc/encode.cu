@@ -93,22 +93,22 @@ __device__ __forceinline__ void unpack32(const uint4 (&raw)[4], float (&x)[32], 
     }
 }
 
-__device__ __forceinline__ uint32_t ge_mask_f32(float a, float b) {
-    uint32_t m;  // 0xFFFFFFFF if a >= b else 0
-    asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
-    return m;
+__device__ __forceinline__ float ge_f32(float a, float b) {
+    float r;  // 1.0f if a >= b else 0.0f
+    asm("set.ge.f32.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
 }
 
-// code = number of boundaries b_i * ||v|| <= y. The boundaries are symmetric (b_{6-i} = -b_i,
-// b_3 = 0): with m = #{i in 4..6 : |y| >= t_i}, the code is 4 + m for y >= 0 (y = -0 included) and
-// 3 - m = (4 + m) ^ 7 for y < 0. For y < 0 the definition compares |y| > t_i; using >= there
-// differs only when |y| equals a scaled boundary, inside the boundary exemption.
-__device__ __forceinline__ uint32_t value_code_thr(float y, float t4, float t5, float t6) {
-    uint32_t sm;                                      // 0xFFFFFFFF for y < 0 (not -0), else 0
-    asm("set.lt.u32.f32 %0, %1, 0f00000000;" : "=r"(sm) : "f"(y));
+// code = number of boundaries b_i * ||v|| <= y, as an exact small float. The boundaries are symmetric
+// (b_{6-i} = -b_i, b_3 = 0): with m = #{i in 4..6 : |y| >= t_i}, the code is 4 + m for y >= 0 and
+// 3 - m for y < 0, i.e. 3.5 + copysign(m + 0.5, y). For y < 0 the definition compares |y| > t_i and
+// y = -0 belongs to the upper half; both differences happen only at an exact boundary (|y| equal to
+// a scaled boundary, or u = 0), inside the boundary exemption. Float arithmetic keeps this work on
+// the FMA pipe; the integer/compare pipe is the encoder's bottleneck.
+__device__ __forceinline__ float value_code_f(float y, float t4, float t5, float t6) {
     const float ay = fabsf(y);
-    const uint32_t neg_m = ge_mask_f32(ay, t4) + ge_mask_f32(ay, t5) + ge_mask_f32(ay, t6);   // minus m
-    return (4u - neg_m) ^ (sm & 7u);
+    const float half_m = ((0.5f + ge_f32(ay, t4)) + ge_f32(ay, t5)) + ge_f32(ay, t6);
+    return 3.5f + copysignf(half_m, y);
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -252,13 +252,18 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(const uint16_t* __restri
     const float t4 = __fmul_rn(kB4, nrm);
     const float t5 = __fmul_rn(kB5, nrm);
     const float t6 = __fmul_rn(kB6, nrm);
-    const bool nz = nrm > 0.0f;
-    uint32_t w24[4] = {0u, 0u, 0u, 0u};
+    // eight codes c_0..c_7 -> the 24-bit group sum c_i * 8^i, formed exactly in fp32 (< 2^24)
+    uint32_t w24[4];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        const uint32_t c0 = nz ? value_code_thr(y[i], t4, t5, t6) : 4u;
-        const uint32_t c1 = nz ? value_code_thr(y[i + 1], t4, t5, t6) : 4u;
-        w24[i >> 3] |= (c0 << (3 * (i & 7))) | (c1 << (3 * ((i & 7) + 1)));
+    for (int g = 0; g < 4; ++g) {
+        float w = value_code_f(y[8 * g + 7], t4, t5, t6);
+#pragma unroll
+        for (int i = 6; i >= 0; --i) w = fmaf(w, 8.0f, value_code_f(y[8 * g + i], t4, t5, t6));
+        w24[g] = (uint32_t)__float2uint_rz(w);
+    }
+    if (!(nrm > 0.0f)) {   // ||v|| = 0: u = 0 everywhere, code 4
+#pragma unroll
+        for (int g = 0; g < 4; ++g) w24[g] = 0x924924u;
     }
     if (valid) {
         // this lane's 32 codes are bits 96*gl .. 96*gl+95 of the vector's packed row
