@@ -55,7 +55,15 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kNR = 64;            // padded rows (MMA N)
-constexpr int kThreadsTc = 576;    // 18 warps
+constexpr int kGroups = 4;                       // softmax row groups
+constexpr int kGRows = kNR / kGroups;            // 16 query rows per group
+constexpr int kSmWarps = 4 * kGroups;            // softmax warps (one per TMEM lane quadrant and group)
+constexpr int kSmThreads = 32 * kSmWarps;
+constexpr int kWarpMma = 8 + kSmWarps;           // MMA issue + TMEM owner
+constexpr int kWarpTma = kWarpMma + 1;
+constexpr int kThreadsTc = 32 * (kWarpTma + 1);  // 26 warps
+// named barriers: 1..4 sync one row group, 5..8 OR-reduce within one (never mixed on an id), 9 all softmax
+constexpr uint32_t kBarGroup = 1, kBarRed = 5, kBarSoftmax = 9;
 constexpr int kNS = 4;             // ring depth: scales / value codes / norms
 constexpr int kKS = 4;             // key-row stages: two per producer group (cp.async, one own tile ahead)
 constexpr float kTau = 8.0f;       // lazy rescale threshold (log2 units): p <= 2^8
@@ -109,8 +117,8 @@ struct Misc {
     float m[kNR];         // running max per row (log2 units); +inf for padding rows
     float nm[kNR];        // -m
     float alpha[kNR];     // 2^(m_old - m_new)
-    float red[2][4][32];
-    float qred[8];
+    float red[kGroups][4][kGRows];   // per (group, lane quadrant, row): partial maxima or row sums
+    float qred[kSmWarps];
     float scale_eff;
     float wscale;
     int abort;
@@ -236,7 +244,7 @@ __device__ __forceinline__ void store_v_quad(const uint32_t (&w)[12], const uint
 __device__ __noinline__ void softmax_new_max(Misc& M, int grp, int tt, int rbase, int R, uint32_t gbar,
                                              bool seg_first, int64_t j, uint32_t lane_addr, volatile int* abortp) {
     tc::named_bar(gbar, 128);
-    if (tt < 32) {
+    if (tt < kGRows) {
         const int r = rbase + tt;
         const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
                                fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
@@ -260,7 +268,7 @@ __device__ __noinline__ void softmax_new_max(Misc& M, int grp, int tt, int rbase
         tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp, kTimeoutNs);
         tc::fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < kGRows / 16; ++cc) {
             uint32_t to[16], tl[16];
             tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
             tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
@@ -285,18 +293,18 @@ __device__ __forceinline__ float unit_wscale(float nmax) {
     return nmax > 0.0f ? ldexpf(1.0f, 8 - en) : 1.0f;
 }
 
-// Segment prologue (both row groups, 256 threads): the unit's queries in fp16 scaled by a power
+// Segment prologue (all row groups, every softmax thread): the unit's queries in fp16 scaled by a power
 // of two into the MMA1 operand, the logit scale and the value scale w.
 template <bool QBF16>
 __device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, const float* __restrict__ nmax, int64_t u,
                                               int r0, int H, int A, int Hq, int G, int R, float scale_log2,
                                               uint8_t* sQ, Misc& M, int si, int wi, int lane) {
     const int layer = (int)(u / H), kvh = (int)(u % H);
-    uint4 qv[4];
+    uint4 qv[1024 / kSmThreads];
     float qm = 0.0f;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int cid = si + 256 * m;
+    for (int m = 0; m < 1024 / kSmThreads; ++m) {
+        const int cid = si + kSmThreads * m;
         qv[m] = make_uint4(0u, 0u, 0u, 0u);
         if (cid < R * 16) {
             const int r = cid >> 4, dc = cid & 15;
@@ -322,16 +330,16 @@ __device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, co
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
     if (lane == 0) M.qred[wi] = qm;
-    tc::named_bar(3, 256);
+    tc::named_bar(kBarSoftmax, kSmThreads);
     float qmax = 0.0f;
 #pragma unroll
-    for (int w8 = 0; w8 < 8; ++w8) qmax = fmaxf(qmax, M.qred[w8]);
+    for (int w8 = 0; w8 < kSmWarps; ++w8) qmax = fmaxf(qmax, M.qred[w8]);
     int eq = 0;
     if (qmax > 0.0f) frexpf(qmax, &eq);
     const float fq = qmax > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;  // qmax * fq in [2^14, 2^15)
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int cid = si + 256 * m;
+    for (int m = 0; m < 1024 / kSmThreads; ++m) {
+        const int cid = si + kSmThreads * m;
         if (cid < kNR * 16) {
             const int r = cid >> 4, dc = cid & 15;
             const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
@@ -360,7 +368,7 @@ __device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, co
         M.wscale = unit_wscale(nmax[u]);
     }
     tc::fence_proxy_async();
-    tc::named_bar(3, 256);
+    tc::named_bar(kBarSoftmax, kSmThreads);
     if (si == 0) tc::mbar_arrive(tc::smem_u32(&M.qready));
 }
 
@@ -374,7 +382,7 @@ __device__ __noinline__ void softmax_epilogue(Misc& M, int s, uint32_t ph, volat
     tc::fence_after();
     tc::wait_st();
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
+    for (int cc = 0; cc < kGRows / 16; ++cc) {
         uint32_t tl[16];
         tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
         tc::wait_ld();
@@ -389,7 +397,7 @@ __device__ __noinline__ void softmax_epilogue(Misc& M, int s, uint32_t ph, volat
     tc::named_bar(gbar, 128);
     const float unscale = 1.0f / M.wscale;
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
+    for (int cc = 0; cc < kGRows / 16; ++cc) {
         uint32_t to[16];
         tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
         tc::wait_ld();
@@ -399,14 +407,14 @@ __device__ __noinline__ void softmax_epilogue(Misc& M, int s, uint32_t ph, volat
             if (r < R) ws_acc[(slot * RS + r) * kD + tt] = __uint_as_float(to[k]) * unscale;
         }
     }
-    if (tt < 32 && rbase + tt < R) {
+    if (tt < kGRows && rbase + tt < R) {
         const int r = rbase + tt;
         ws_ml[(slot * RS + r) * 2] = M.m[r];
         ws_ml[(slot * RS + r) * 2 + 1] =
             M.red[grp][0][tt] + M.red[grp][1][tt] + M.red[grp][2][tt] + M.red[grp][3][tt];
     }
     tc::fence_before();
-    tc::named_bar(3, 256);
+    tc::named_bar(kBarSoftmax, kSmThreads);
 }
 
 template <bool QBF16>
@@ -439,10 +447,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc::mbar_init(tc::smem_u32(&M.kfull[s]), 128);
             tc::mbar_init(tc::smem_u32(&M.kfree[s]), 1);
             tc::mbar_init(tc::smem_u32(&M.vfull[s]), 128);
-            tc::mbar_init(tc::smem_u32(&M.pfull[s]), 256);
+            tc::mbar_init(tc::smem_u32(&M.pfull[s]), kSmThreads);
             tc::mbar_init(tc::smem_u32(&M.pvfree[s]), 1);
             tc::mbar_init(tc::smem_u32(&M.sfull[s]), 1);
-            tc::mbar_init(tc::smem_u32(&M.sfree[s]), 256);
+            tc::mbar_init(tc::smem_u32(&M.sfree[s]), kSmThreads);
         }
         for (int s = 0; s < kNS; ++s) {
             tc::mbar_init(tc::smem_u32(&M.rfull[s]), 1);
@@ -459,13 +467,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const __half hi = __float2half_rn(centroid_of(idx >> 3));
         lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
     }
-    if (warp == 16) tc::tmem_alloc(tc::smem_u32(&M.tslot), kTmemCols);
+    if (warp == kWarpMma) tc::tmem_alloc(tc::smem_u32(&M.tslot), kTmemCols);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tbase = M.tslot;
 
-    if (warp == 17) {
+    if (warp == kWarpTma) {
         // =============================== TMA: scales / value codes / norms into the ring
         if (lane == 0) {
             int issued = 0;
@@ -620,16 +628,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (u != u_prev && j + 2 < n) wscale = unit_wscale(P.p.nmax[u / P.nrg]);
         }
         cp_async_wait<0>();   // no copy may land in shared memory after the CTA exits
-    } else if (warp < 16) {
-        // =============================== softmax + epilogue (two groups of 32 rows)
-        const int grp = (warp - 8) >> 2;        // row group: rows 32*grp .. 32*grp+31
+    } else if (warp < 8 + kSmWarps) {
+        // =============================== softmax + epilogue (four groups of 16 rows)
+        const int grp = (warp - 8) >> 2;        // row group: rows 16*grp .. 16*grp+15
         const int wq = warp & 3;                // TMEM lane quadrant
         const int tt = wq * 32 + lane;          // token slot = TMEM lane (= head-dim index in the epilogue)
-        const int si = tid - 256;               // 0..255 over both groups
+        const int si = tid - 256;               // 0 .. kSmThreads-1 over all groups
         const uint32_t lane_addr = tbase + ((uint32_t)(wq * 32) << 16);
-        const uint32_t gbar = 1 + grp;
+        const uint32_t gbar = kBarGroup + grp;
         int R = 0;                               // rows of the current segment
-        const int rbase = 32 * grp;
+        const int rbase = kGRows * grp;
         int seg = -1;
         int64_t seg_u = -1;
         int64_t u = g0 / nt;
@@ -667,87 +675,67 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const float scale_eff = M.scale_eff;
             const bool tail = (int64_t)(ti + 1) * kTile > P.n_ctx;
             const bool valid = (int64_t)ti * kTile + tt < P.n_ctx;
-            // -------- logits for this group's 32 rows, d = c * S - m, recomputed from TMEM in each pass
-            // (absolute c * S on a segment's first tile, before the running max exists)
+            // -------- logits for this group's 16 rows, d = c * S - m (absolute c * S on a segment's
+            // first tile, before the running max exists). S and the per-slot row sums come from TMEM in
+            // one round trip and stay in registers; if a new running max is needed (the segment's first
+            // tile, or a logit above the max by more than 2^tau) the max is updated and the tile is
+            // read again against it, so no tile data is live across the out-of-line update.
             const float2 c2 = make_float2(scale_eff, scale_eff);
-            auto logits16 = [&](int cc, float2 (&d2)[8], bool absolute) {
-                uint32_t t0[16];
-                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase + 16u * cc, t0);
-                tc::wait_ld();
-                const float2* nm2 = reinterpret_cast<const float2*>(&M.nm[rbase + 16 * cc]);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 sv = make_float2(__uint_as_float(t0[2 * k]), __uint_as_float(t0[2 * k + 1]));
-                    d2[k] = absolute ? mul2(c2, sv) : fma2(c2, sv, nm2[k]);
-                }
-                if (tail && !valid) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) d2[k] = make_float2(-INFINITY, -INFINITY);
-                }
-            };
             tc::mbar_wait(tc::smem_u32(&M.sfull[s]), ph, abortp, kTimeoutNs);
             tc::fence_after();
-            // -------- lazy rescale: only when some logit exceeds the running max by more than 2^tau
-            bool need = first;
-            if (!first) {
+            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
+            uint32_t sd[16], ls[16];   // S, then d, as float bits; per-slot row sums
+            bool absolute = first;
+            for (;;) {
+                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase, sd);
+                if (!first) tc::tmem_ld16(lane_addr + kColL + rbase, ls);
+                tc::wait_ld();
+                if (first) {   // a segment starts its row sums at zero
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) ls[k] = 0u;
+                }
+                const float2* nm2 = reinterpret_cast<const float2*>(&M.nm[rbase]);
                 float dmax = -INFINITY;
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float2 d2[8];
-                    logits16(cc, d2, false);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) dmax = fmaxf(dmax, fmaxf(d2[k].x, d2[k].y));
+                for (int k = 0; k < 8; ++k) {
+                    const float2 sv = make_float2(__uint_as_float(sd[2 * k]), __uint_as_float(sd[2 * k + 1]));
+                    float2 d = absolute ? mul2(c2, sv) : fma2(c2, sv, nm2[k]);
+                    if (tail && !valid) d = make_float2(-INFINITY, -INFINITY);
+                    dmax = fmaxf(dmax, fmaxf(d.x, d.y));
+                    sd[2 * k] = __float_as_uint(d.x);
+                    sd[2 * k + 1] = __float_as_uint(d.y);
                 }
-                // ids 4, 5: a reducing barrier never shares its id with the bar.sync barriers (1, 2)
-                need = bar_any(gbar + 3, 128, dmax > kTau);
-            }
-            if (need) {
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float2 d2[8];
-                    logits16(cc, d2, first);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float v0 = tc::warp_max(d2[k].x);
-                        const float v1 = tc::warp_max(d2[k].y);
-                        if (lane == 16 * cc + 2 * k) M.red[grp][wq][16 * cc + 2 * k] = v0;
-                        if (lane == 16 * cc + 2 * k + 1) M.red[grp][wq][16 * cc + 2 * k + 1] = v1;
-                    }
-                }
-                softmax_new_max(M, grp, tt, rbase, R, gbar, first, j, lane_addr, abortp);
-            }
-            // -------- probabilities p = 2^d (fp16) and running sums, against the (new) running max
-            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
-            const uint32_t prow = tc::smem_u32(sP) + s * 16384;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t tl[16];
-                if (!first) tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
-                float2 d2[8];
-                logits16(cc, d2, false);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 4 * half + e;
-                        d2[k] = make_float2(ex2(d2[k].x), ex2(d2[k].y));  // d2 now holds p
-                        const __half2 h = __floats2half2_rn(d2[k].x, d2[k].y);
-                        pk[e] = *reinterpret_cast<const uint32_t*>(&h);
-                    }
-                    st_shared16(prow + tc::sw128((uint32_t)tt, 16u * (4 * grp + 2 * cc + half)), pk[0], pk[1], pk[2],
-                                pk[3]);
-                }
+                const bool need = absolute || bar_any(kBarRed + grp, 128, dmax > kTau);
+                if (!need) break;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    float2 l = first ? make_float2(0.0f, 0.0f)
-                                     : make_float2(__uint_as_float(tl[2 * k]), __uint_as_float(tl[2 * k + 1]));
-                    l = add2(l, d2[k]);
-                    tl[2 * k] = __float_as_uint(l.x);
-                    tl[2 * k + 1] = __float_as_uint(l.y);
+                    const float v0 = tc::warp_max(__uint_as_float(sd[2 * k]));
+                    const float v1 = tc::warp_max(__uint_as_float(sd[2 * k + 1]));
+                    if (lane == 2 * k) M.red[grp][wq][2 * k] = v0;
+                    if (lane == 2 * k + 1) M.red[grp][wq][2 * k + 1] = v1;
                 }
-                tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
+                softmax_new_max(M, grp, tt, rbase, R, gbar, absolute, j, lane_addr, abortp);
+                absolute = false;   // the second pass sees every logit at or below the new max
             }
+            // -------- probabilities p = 2^d (fp16) and running sums
+            const uint32_t prow = tc::smem_u32(sP) + s * 16384;
+#pragma unroll
+            for (int c8 = 0; c8 < 2; ++c8) {   // 8 rows per 16-byte chunk
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 4 * c8 + e;
+                    const float p0 = ex2(__uint_as_float(sd[2 * k])), p1 = ex2(__uint_as_float(sd[2 * k + 1]));
+                    const __half2 h = __floats2half2_rn(p0, p1);
+                    pk[e] = *reinterpret_cast<const uint32_t*>(&h);
+                    const float2 l =
+                        add2(make_float2(__uint_as_float(ls[2 * k]), __uint_as_float(ls[2 * k + 1])), make_float2(p0, p1));
+                    ls[2 * k] = __float_as_uint(l.x);
+                    ls[2 * k + 1] = __float_as_uint(l.y);
+                }
+                st_shared16(prow + tc::sw128((uint32_t)tt, 16u * (2 * grp + c8)), pk[0], pk[1], pk[2], pk[3]);
+            }
+            tc::tmem_st16(lane_addr + kColL + rbase, ls);
             tc::fence_before();
             tc::mbar_arrive(tc::smem_u32(&M.sfree[s]));   // S has been read for the last time
             tc::fence_proxy_async();
@@ -759,7 +747,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                                  P.ws_acc, P.ws_ml);
             }
         }
-    } else if (warp == 16 && lane == 0) {
+    } else if (warp == kWarpMma && lane == 0) {
         // =============================== MMA issuer (one thread): an event loop over both chains
         const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);
         const uint32_t id2 = tc::idesc_f16(128, kNR, true, true);
@@ -834,7 +822,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ---- tear-down: every role is past its last TMEM access
     tc::fence_before();
     __syncthreads();
-    if (warp == 16) {
+    if (warp == kWarpMma) {
         tc::fence_after();
         tc::tmem_dealloc(tbase, kTmemCols);
     }
