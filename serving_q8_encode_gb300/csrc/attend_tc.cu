@@ -751,7 +751,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // =============================== MMA issuer (one thread): an event loop over both chains
         const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);
         const uint32_t id2 = tc::idesc_f16(128, kNR, true, true);
-        const uint32_t sq = tc::smem_u32(sQ), sv = tc::smem_u32(sV), sp = tc::smem_u32(sP);
+        // Shared-memory descriptors, built once: the start-address field holds address >> 4, so a
+        // k-step or stage offset is added to the descriptor itself (every operand is below 256 KB).
+        // The issuing thread shares its SM sub-partition with six other warps; every instruction it
+        // saves per MMA shortens the tile.
+        uint64_t bq[8];
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) bq[ks] = tc::sdesc(tc::smem_u32(sQ) + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
+        const uint64_t av0 = tc::sdesc(tc::smem_u32(sV), 16384, 1024);
+        const uint64_t bp0 = tc::sdesc(tc::smem_u32(sP), 16384, 1024);
+        const uint32_t tS = tbase + kColS, tK = tbase + kColK, tO = tbase + kColO;
         int j1 = 0, j2 = 0;        // next MMA1 / MMA2 tile
         int seg1 = 0;              // segments whose first MMA1 has been issued
         int ti1 = (int)(g0 % nt), ti2 = ti1;
@@ -766,14 +775,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     tc::mbar_try(tc::smem_u32(&M.kfull[s]), (uint32_t)((j1 >> 1) & 1)) &&
                     (j1 < 2 || tc::mbar_try(tc::smem_u32(&M.sfree[s]), (uint32_t)(((j1 - 2) >> 1) & 1)))) {
                     tc::fence_after();
+                    const uint32_t dS = tS + 64u * s, aK = tK + 128u * s;
+                    tc::mma_ts_c<0>(dS, aK, bq[0], id1);   // hi then lo halves of the scaled keys
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)   // hi then lo halves of the scaled keys
+                    for (int ks = 1; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 8u * ks, bq[ks], id1);
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint64_t bd = tc::sdesc(sq + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
-                            tc::mma_ts(tbase + kColS + 64u * s, tbase + kColK + 128u * s + 64u * part + 8u * ks, bd,
-                                       id1, (part | ks) ? 1u : 0u);
-                        }
+                    for (int ks = 0; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 64u + 8u * ks, bq[ks], id1);
                     tc::commit(tc::smem_u32(&M.sfull[s]));
                     tc::commit(tc::smem_u32(&M.kfree[s]));
                     if (f1) ++seg1;
@@ -788,12 +795,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 if (tc::mbar_try(tc::smem_u32(&M.vfull[s2]), ph2) && tc::mbar_try(tc::smem_u32(&M.pfull[s2]), ph2)) {
                     const bool f2 = (j2 == 0) || (ti2 == 0);
                     tc::fence_after();
+                    const uint64_t ad = av0 + (uint64_t)(s2 * (32768 >> 4));
+                    const uint64_t bd = bp0 + (uint64_t)(s2 * (16384 >> 4));
+                    if (f2)
+                        tc::mma_ss_c<0>(tO, ad, bd, id2);
+                    else
+                        tc::mma_ss_c<1>(tO, ad, bd, id2);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t ad = tc::sdesc(sv + s2 * 32768 + ks * 2048, 16384, 1024);
-                        const uint64_t bd = tc::sdesc(sp + s2 * 16384 + ks * 2048, 16384, 1024);
-                        tc::mma_ss(tbase + kColO, ad, bd, id2, (f2 && ks == 0) ? 0u : 1u);
-                    }
+                    for (int ks = 1; ks < 8; ++ks)
+                        tc::mma_ss_c<1>(tO, ad + (uint64_t)(ks * (2048 >> 4)), bd + (uint64_t)(ks * (2048 >> 4)), id2);
                     tc::commit(tc::smem_u32(&M.pvfree[s2]));
                     if (++ti2 == nt) ti2 = 0;
                     ++j2;
