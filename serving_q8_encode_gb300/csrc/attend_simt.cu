@@ -270,17 +270,51 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
 // from a contiguous cut of the (unit, tile) list into nc ranges (tt tiles,
 // nt per unit) and unit u has one piece per range that overlaps it;
 // otherwise every unit has n_slots pieces.
+//
+// The kernel is bound by load latency (the partials were just written and
+// sit in L2), so each lane issues the loads of up to kMergeBatch pieces, and
+// of the suffix partial, before it uses any of them, with one vector load
+// per piece, and folds each batch into a running maximum.
+constexpr int kMergeBatch = 4;
+constexpr int kMergeWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
-                                                    float* __restrict__ out, int U, int H, int A, int Hq, int R,
-                                                    int n_slots, MergeLayout lay,
-                                                    const float* __restrict__ sfx_acc,
-                                                    const float* __restrict__ sfx_ml) {
+struct MergeVec;
+template <>
+struct MergeVec<128> {
+    using T = float4;
+    static __device__ __forceinline__ void to(const T& v, float* o) { o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w; }
+    static __device__ __forceinline__ T from(const float* o) { return make_float4(o[0], o[1], o[2], o[3]); }
+};
+template <>
+struct MergeVec<64> {
+    using T = float2;
+    static __device__ __forceinline__ void to(const T& v, float* o) { o[0] = v.x; o[1] = v.y; }
+    static __device__ __forceinline__ T from(const float* o) { return make_float2(o[0], o[1]); }
+};
+
+// First tile-range index overlapping tile position x of the (unit, tile) list
+// cut into nc ranges of tt tiles: floor((x * nc - 1) / tt) for x >= 1. Uses
+// 32-bit division when the product fits, which is the usual case.
+__device__ __forceinline__ int64_t merge_range_of(int64_t x, int nc, int64_t tt) {
+    const int64_t num = x * nc - 1;
+    if (num <= 0xFFFFFFFFll && tt <= 0xFFFFFFFFll) return (int64_t)((uint32_t)num / (uint32_t)tt);
+    return num / tt;
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * kMergeWarps) attend_merge(const float* __restrict__ ws_acc,
+                                                                 const float* __restrict__ ws_ml,
+                                                                 float* __restrict__ out, int U, int H, int A, int Hq,
+                                                                 int R, int n_slots, MergeLayout lay,
+                                                                 const float* __restrict__ sfx_acc,
+                                                                 const float* __restrict__ sfx_ml) {
     constexpr int EPL = D / 32;  // elements per lane
-    const int wid = blockIdx.x * 4 + threadIdx.x / 32;
+    using V = MergeVec<D>;
+    const int64_t wid = (int64_t)blockIdx.x * kMergeWarps + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if ((int64_t)wid >= (int64_t)U * R) return;
-    const int unit = wid / R, r = wid % R;
+    if (wid >= (int64_t)U * R) return;
+    const int unit = (int)(wid / R), r = (int)(wid % R);
     const int G = Hq / H;
     const int layer = unit / H, kvh = unit % H;
     const int a = r / G, g = r % G;
@@ -290,29 +324,57 @@ __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws
     int64_t first = (int64_t)unit * n_slots * R + r, stride = R;
     if (lay.nc > 0) {
         const int64_t seg = (int64_t)unit * lay.nrg + r / lay.RS;
-        const int64_t lo = ((seg * lay.nt + 1) * lay.nc - 1) / lay.tt;
-        const int64_t hi = ((seg * lay.nt + lay.nt) * lay.nc - 1) / lay.tt;
+        const int64_t lo = merge_range_of(seg * lay.nt + 1, lay.nc, lay.tt);
+        const int64_t hi = merge_range_of(seg * lay.nt + lay.nt, lay.nc, lay.tt);
         pieces = (int)(hi - lo + 1);
         first = (seg + lo) * lay.RS + r % lay.RS;
         stride = lay.RS;
     }
     const int64_t orow = ((int64_t)layer * A + a) * Hq + kvh * G + g;   // output / suffix row
-    float M = -INFINITY;
-    for (int s = 0; s < pieces; ++s) M = fmaxf(M, ws_ml[(first + s * stride) * 2]);
-    if (sfx_ml) M = fmaxf(M, sfx_ml[orow * 2]);
-    float L = 0.0f;
+
+    // the suffix partial is independent of the pieces: start its loads first
+    float2 sml = make_float2(-INFINITY, 0.0f);
+    typename V::T sv{};
+    if (sfx_ml) {
+        sml = reinterpret_cast<const float2*>(sfx_ml)[orow];
+        sv = reinterpret_cast<const typename V::T*>(sfx_acc + orow * D)[lane];
+    }
+
+    float M = -INFINITY, L = 0.0f;
     float o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
-    for (int s = 0; s < pieces; ++s) {
-        const int64_t pr = first + s * stride;
-        const float ms = ws_ml[pr * 2];
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - M);
-        L = fmaf(w, ws_ml[pr * 2 + 1], L);
-        const float* src = ws_acc + pr * D + lane * EPL;
+    for (int s0 = 0; s0 < pieces; s0 += kMergeBatch) {
+        float2 ml[kMergeBatch];
+        typename V::T v[kMergeBatch];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, src[e], o[e]);
+        for (int i = 0; i < kMergeBatch; ++i) {
+            ml[i] = make_float2(-INFINITY, 0.0f);
+            if (s0 + i < pieces) {
+                const int64_t pr = first + (int64_t)(s0 + i) * stride;
+                ml[i] = reinterpret_cast<const float2*>(ws_ml)[pr];
+                v[i] = reinterpret_cast<const typename V::T*>(ws_acc + pr * D)[lane];
+            }
+        }
+        float Mn = M;
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) Mn = fmaxf(Mn, ml[i].x);
+        if (Mn == -INFINITY) continue;
+        const float c = exp2f(M - Mn);  // 0 while nothing has been merged
+        L *= c;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] *= c;
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            if (ml[i].x == -INFINITY) continue;
+            const float w = exp2f(ml[i].x - Mn);
+            L = fmaf(w, ml[i].y, L);
+            float x[EPL];
+            V::to(v[i], x);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, x[e], o[e]);
+        }
+        M = Mn;
     }
     // in-lane butterflies (strides < EPL), then across lanes
 #pragma unroll
@@ -335,21 +397,20 @@ __global__ void __launch_bounds__(128) attend_merge(const float* __restrict__ ws
     }
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= (1.0f / D);
-    if (sfx_ml) {
+    if (sml.x != -INFINITY) {
         // the suffix partial is already in the original basis
-        const float ms = sfx_ml[orow * 2];
-        if (ms != -INFINITY) {
-            const float w = exp2f(ms - M);
-            L = fmaf(w, sfx_ml[orow * 2 + 1], L);
-            const float* src = sfx_acc + orow * D + lane * EPL;
+        const float Mn = fmaxf(M, sml.x);
+        const float c = exp2f(M - Mn), w = exp2f(sml.x - Mn);
+        float x[EPL];
+        V::to(sv, x);
+        L = fmaf(w, sml.y, L * c);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, src[e], o[e]);
-        }
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, x[e], o[e] * c);
     }
     const float inv = 1.0f / L;
-    float* dst = out + orow * D + lane * EPL;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) dst[e] = o[e] * inv;
+    for (int e = 0; e < EPL; ++e) o[e] *= inv;
+    reinterpret_cast<typename V::T*>(out + orow * D)[lane] = V::from(o);
 }
 
 template <int D, int RMAX, bool BF16>
@@ -403,11 +464,11 @@ polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float
                                   int R, int n_slots, const MergeLayout& lay, int D, cudaStream_t st,
                                   const float* sfx_acc, const float* sfx_ml) {
     const int64_t warps = (int64_t)U * R;
-    const unsigned blocks = (unsigned)((warps + 3) / 4);
+    const unsigned blocks = (unsigned)((warps + kMergeWarps - 1) / kMergeWarps);
     if (D == 128)
-        attend_merge<128><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
+        attend_merge<128><<<blocks, 32 * kMergeWarps, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
     else
-        attend_merge<64><<<blocks, 128, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
+        attend_merge<64><<<blocks, 32 * kMergeWarps, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend merge launch: %s", cudaGetErrorString(e));
     return POLYKV_OK;

@@ -747,14 +747,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                                  P.ws_acc, P.ws_ml);
             }
         }
-    } else if (warp == kWarpMma && lane == 0) {
-        // =============================== MMA issuer (one thread): an event loop over both chains
+    } else if (warp == kWarpMma) {
+        // =============================== MMA issuer: an event loop over both chains
+        // The whole warp runs the loop with warp-uniform control (barrier tests broadcast from lane
+        // 0) and one elected lane issues the MMAs and commits. Issuing from a converged warp instead
+        // of a single-lane branch cut the tile period by about a tenth.
         const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);
         const uint32_t id2 = tc::idesc_f16(128, kNR, true, true);
         // Shared-memory descriptors, built once: the start-address field holds address >> 4, so a
         // k-step or stage offset is added to the descriptor itself (every operand is below 256 KB).
-        // The issuing thread shares its SM sub-partition with six other warps; every instruction it
+        // The issuing warp shares its SM sub-partition with six other warps; every instruction it
         // saves per MMA shortens the tile.
+        const bool leader = tc::elect_one();
         uint64_t bq[8];
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) bq[ks] = tc::sdesc(tc::smem_u32(sQ) + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
@@ -771,18 +775,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (j1 < n) {
                 const int s = j1 & 1;
                 const bool f1 = (j1 == 0) || (ti1 == 0);
-                if ((!f1 || tc::mbar_try(tc::smem_u32(&M.qready), (uint32_t)(seg1 & 1))) &&
-                    tc::mbar_try(tc::smem_u32(&M.kfull[s]), (uint32_t)((j1 >> 1) & 1)) &&
-                    (j1 < 2 || tc::mbar_try(tc::smem_u32(&M.sfree[s]), (uint32_t)(((j1 - 2) >> 1) & 1)))) {
+                const bool r1 = (!f1 || tc::mbar_test(tc::smem_u32(&M.qready), (uint32_t)(seg1 & 1))) &&
+                                tc::mbar_test(tc::smem_u32(&M.kfull[s]), (uint32_t)((j1 >> 1) & 1)) &&
+                                (j1 < 2 || tc::mbar_test(tc::smem_u32(&M.sfree[s]), (uint32_t)(((j1 - 2) >> 1) & 1)));
+                if (__shfl_sync(0xffffffffu, r1 ? 1 : 0, 0)) {
                     tc::fence_after();
                     const uint32_t dS = tS + 64u * s, aK = tK + 128u * s;
-                    tc::mma_ts_c<0>(dS, aK, bq[0], id1);   // hi then lo halves of the scaled keys
+                    if (leader) {
+                        tc::mma_ts_c<0>(dS, aK, bq[0], id1);   // hi then lo halves of the scaled keys
 #pragma unroll
-                    for (int ks = 1; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 8u * ks, bq[ks], id1);
+                        for (int ks = 1; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 8u * ks, bq[ks], id1);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 64u + 8u * ks, bq[ks], id1);
-                    tc::commit(tc::smem_u32(&M.sfull[s]));
-                    tc::commit(tc::smem_u32(&M.kfree[s]));
+                        for (int ks = 0; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 64u + 8u * ks, bq[ks], id1);
+                        tc::commit(tc::smem_u32(&M.sfull[s]));
+                        tc::commit(tc::smem_u32(&M.kfree[s]));
+                    }
                     if (f1) ++seg1;
                     if (++ti1 == nt) ti1 = 0;
                     ++j1;
@@ -792,19 +799,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (j2 < j1) {
                 const int s2 = j2 & 1;
                 const uint32_t ph2 = (uint32_t)((j2 >> 1) & 1);
-                if (tc::mbar_try(tc::smem_u32(&M.vfull[s2]), ph2) && tc::mbar_try(tc::smem_u32(&M.pfull[s2]), ph2)) {
+                const bool r2 = tc::mbar_test(tc::smem_u32(&M.vfull[s2]), ph2) && tc::mbar_test(tc::smem_u32(&M.pfull[s2]), ph2);
+                if (__shfl_sync(0xffffffffu, r2 ? 1 : 0, 0)) {
                     const bool f2 = (j2 == 0) || (ti2 == 0);
                     tc::fence_after();
                     const uint64_t ad = av0 + (uint64_t)(s2 * (32768 >> 4));
                     const uint64_t bd = bp0 + (uint64_t)(s2 * (16384 >> 4));
-                    if (f2)
-                        tc::mma_ss_c<0>(tO, ad, bd, id2);
-                    else
-                        tc::mma_ss_c<1>(tO, ad, bd, id2);
+                    if (leader) {
+                        if (f2)
+                            tc::mma_ss_c<0>(tO, ad, bd, id2);
+                        else
+                            tc::mma_ss_c<1>(tO, ad, bd, id2);
 #pragma unroll
-                    for (int ks = 1; ks < 8; ++ks)
-                        tc::mma_ss_c<1>(tO, ad + (uint64_t)(ks * (2048 >> 4)), bd + (uint64_t)(ks * (2048 >> 4)), id2);
-                    tc::commit(tc::smem_u32(&M.pvfree[s2]));
+                        for (int ks = 1; ks < 8; ++ks)
+                            tc::mma_ss_c<1>(tO, ad + (uint64_t)(ks * (2048 >> 4)), bd + (uint64_t)(ks * (2048 >> 4)), id2);
+                        tc::commit(tc::smem_u32(&M.pvfree[s2]));
+                    }
                     if (++ti2 == nt) ti2 = 0;
                     ++j2;
                     prog = true;
@@ -813,17 +823,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (prog) {
                 t_last = tc::globaltimer();
             } else {
-                if (*abortp) break;
-                if (tc::globaltimer() - t_last > kTimeoutNs) {
-                    *abortp = 1;
-                    break;
-                }
+                // lane 0 decides, so the warp leaves the loop together
+                const int stop = *abortp ? 1 : (tc::globaltimer() - t_last > kTimeoutNs ? 2 : 0);
+                const int stop0 = __shfl_sync(0xffffffffu, stop, 0);
+                if (stop0 == 2 && lane == 0) *abortp = 1;
+                if (stop0) break;
             }
         }
         if (P.test_stall) *abortp = 0;  // let the other roles discover the stall on their own waits
         if (j1 > 0) {
-            // every MMA this thread issued must have completed before the TMEM is freed
-            tc::commit(tc::smem_u32(&M.done));
+            // every MMA this warp issued must have completed before the TMEM is freed
+            if (leader) tc::commit(tc::smem_u32(&M.done));
             volatile int dummy = 0;
             tc::mbar_wait(tc::smem_u32(&M.done), 0u, &dummy, 50000000ull);
         }

@@ -20,10 +20,10 @@
 //   keys:   x (bf16/fp16) and s16 have short significands, so x / s16 is either
 //           exactly a half-integer or at least 2^-13 away from every
 //           half-integer (x and s16 are small odd integers times powers of
-//           two); x * RN(1/s16) is within 2^-15 of x / s16 (|x / s16| < 2^8),
-//           so floor(|x * y| + 0.5 + 2^-14) picks the same code as rounding
-//           the exact (or correctly rounded) quotient, ties away from zero
-//           included; then the [-127, 127] clamp;
+//           two). With a normal scale the code is the integer nearest to
+//           x * yb, yb a hair above 1 / s16, read from the mantissa of one
+//           fused multiply-add (details at the key step); a zero, subnormal or
+//           non-finite scale takes a slower path with the [-127, 127] clamp;
 //   values: u >= b  <=>  y >= b * ||v|| except when u is within a few ulps of b
 //           (where the rounding of either side can flip the comparison); such
 //           boundary cases are the only ones allowed to differ from the
@@ -99,21 +99,24 @@ __device__ __forceinline__ float ge_f32(float a, float b) {
     return r;
 }
 
-// code = number of boundaries b_i * ||v|| <= y, as an exact small float. The boundaries are symmetric
-// (b_{6-i} = -b_i, b_3 = 0): with m = #{i in 4..6 : |y| >= t_i}, the code is 4 + m for y >= 0 and
-// 3 - m for y < 0, i.e. 3.5 + copysign(m + 0.5, y). For y < 0 the definition compares |y| > t_i and
-// y = -0 belongs to the upper half; both differences happen only at an exact boundary (|y| equal to
-// a scaled boundary, or u = 0), inside the boundary exemption. Float arithmetic keeps this work on
-// the FMA pipe; the integer/compare pipe is the encoder's bottleneck.
-__device__ __forceinline__ float value_code_f(float y, float t4, float t5, float t6) {
+// code = number of boundaries b_i * ||v|| <= y. The boundaries are symmetric (b_{6-i} = -b_i,
+// b_3 = 0): with m = #{i in 4..6 : |y| >= t_i}, the code is 4 + m for y >= 0 and 3 - m for y < 0,
+// i.e. 3.5 + copysign(m + 0.5, y). This returns the signed half-code copysign(m + 0.5, y) = code - 3.5
+// as an exact float; the caller adds the 3.5s of a whole group at once. For y < 0 the definition
+// compares |y| > t_i and y = -0 belongs to the upper half; both differences happen only at an exact
+// boundary (|y| equal to a scaled boundary, or u = 0), inside the boundary exemption. Float
+// arithmetic keeps this work on the FMA pipe; the integer/compare pipe is the encoder's bottleneck.
+__device__ __forceinline__ float value_half_code(float y, float t4, float t5, float t6) {
     const float ay = fabsf(y);
     const float half_m = ((0.5f + ge_f32(ay, t4)) + ge_f32(ay, t5)) + ge_f32(ay, t6);
-    return 3.5f + copysignf(half_m, y);
+    return copysignf(half_m, y);
 }
 
+// three-input maximum that returns NaN if any input is NaN (a block holding a NaN then gets a NaN
+// scale and all-zero codes, as when the maximum is taken with NaN propagation)
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
 
@@ -159,27 +162,39 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(const uint16_t* __restri
         for (int i = 0; i < 32; i += 2) amax = max3(amax, fabsf(x[i]), fabsf(x[i + 1]));
         const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
         const float sf = __half2float(s16);
-        // a block whose scale is 0 or not finite gets zero codes (y = 0 makes every x * y zero)
-        const bool usable = sf > 0.0f && sf <= 65504.0f;
-        const float yb = usable ? __frcp_rn(sf) : 0.0f;
-        const float2 yb2 = make_float2(yb, yb);
         uint32_t packed[8];
-        // round half away from zero: trunc(RN(x * y) +- (0.5 + 2^-14)) with the addition rounded
-        // toward zero; with a normal scale |x / s16| <= 127.06, so no clamp is needed, while a
-        // subnormal scale can take it up to ~189 and the code is clamped to [-127, 127]
-        const bool clamp = !(sf >= 6.103515625e-05f);
+        if (sf >= 6.103515625e-05f && sf <= 65504.0f) {
+            // normal scale: the code is the integer nearest to x * yb, read from the low byte of
+            // RN(x * yb + (2^23 + 256)), one fused multiply-add per element. yb is one ulp above
+            // RU(1 / s16), so x * yb = (x / s16)(1 + e) with 0 < e <= 2^-22: an exact half-integer
+            // quotient moves away from zero (ties away), and any other quotient, at least 2^-13 from
+            // every half-integer, moves by at most 127.06 * 2^-22 < 2^-13 and keeps its nearest
+            // integer. The sum lies in [2^23, 2^24), where RN rounds to an integer and the mantissa
+            // holds 256 + code, whose low byte is the int8 code. |x / s16| <= 127.06: no clamp.
+            const float yb = __uint_as_float(__float_as_uint(__frcp_ru(sf)) + 1u);
+            const float2 yb2 = make_float2(yb, yb);
+            const float2 mg2 = make_float2(8388864.0f, 8388864.0f);   // 2^23 + 256
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float2 r01 = mul2(make_float2(x[i], x[i + 1]), yb2);
-            const float2 r23 = mul2(make_float2(x[i + 2], x[i + 3]), yb2);
-            int q0 = round_away(r01.x), q1 = round_away(r01.y), q2 = round_away(r23.x), q3 = round_away(r23.y);
-            if (clamp) {
-                q0 = max(-127, min(127, q0));
-                q1 = max(-127, min(127, q1));
-                q2 = max(-127, min(127, q2));
-                q3 = max(-127, min(127, q3));
+            for (int i = 0; i < 32; i += 4) {
+                const float2 r01 = fma2(make_float2(x[i], x[i + 1]), yb2, mg2);
+                const float2 r23 = fma2(make_float2(x[i + 2], x[i + 3]), yb2, mg2);
+                packed[i >> 2] = bytes4(__float_as_int(r01.x), __float_as_int(r01.y), __float_as_int(r23.x),
+                                        __float_as_int(r23.y));
             }
-            packed[i >> 2] = bytes4(q0, q1, q2, q3);
+        } else {
+            // zero, subnormal or non-finite scale: round half away from zero as
+            // trunc(RN(x * RN(1/s16)) +- (0.5 + 2^-14)) with the addition rounded toward zero, then
+            // the [-127, 127] clamp (a subnormal scale can take |x / s16| up to ~189); a scale that
+            // is 0 or not finite gives y = 0 and all-zero codes
+            const bool usable = sf > 0.0f && sf <= 65504.0f;
+            const float yb = usable ? __frcp_rn(sf) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                int q[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) q[e] = max(-127, min(127, round_away(__fmul_rn(x[i + e], yb))));
+                packed[i >> 2] = bytes4(q[0], q[1], q[2], q[3]);
+            }
         }
         if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.kq + pidx * D + gl * 32);
@@ -252,14 +267,17 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(const uint16_t* __restri
     const float t4 = __fmul_rn(kB4, nrm);
     const float t5 = __fmul_rn(kB5, nrm);
     const float t6 = __fmul_rn(kB6, nrm);
-    // eight codes c_0..c_7 -> the 24-bit group sum c_i * 8^i, formed exactly in fp32 (< 2^24)
+    // eight codes c_0..c_7 -> the 24-bit group sum c_i * 8^i, formed exactly in fp32: Horner over the
+    // half-codes h_i = c_i - 3.5 gives sum h_i 8^i, a multiple of 1/2 below 2^23 in magnitude (24
+    // significant bits at most, so every step is exact); adding 3.5 * sum 8^i = 8388607.5 gives the
+    // integer group sum (< 2^24), also exactly
     uint32_t w24[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        float w = value_code_f(y[8 * g + 7], t4, t5, t6);
+        float w = value_half_code(y[8 * g + 7], t4, t5, t6);
 #pragma unroll
-        for (int i = 6; i >= 0; --i) w = fmaf(w, 8.0f, value_code_f(y[8 * g + i], t4, t5, t6));
-        w24[g] = (uint32_t)__float2uint_rz(w);
+        for (int i = 6; i >= 0; --i) w = fmaf(w, 8.0f, value_half_code(y[8 * g + i], t4, t5, t6));
+        w24[g] = (uint32_t)__float2uint_rz(w + 8388607.5f);
     }
     if (!(nrm > 0.0f)) {   // ||v|| = 0: u = 0 everywhere, code 4
 #pragma unroll

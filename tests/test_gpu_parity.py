@@ -214,6 +214,34 @@ def test_tiny_key_blocks_subnormal_scales(env):
     check_encode(pool, ref, T, 0, b32)
 
 
+def test_non_finite_key_blocks(env):
+    """A key block holding an inf or a NaN gets a non-finite scale and all-zero codes (the
+    oracle's reading); every other block and all values stay bit-exact."""
+    pk, torch, c32, b32 = env
+    L, H, d, T = 1, 1, 128, 8
+    rng = np.random.default_rng(5)
+    k = rng.standard_normal((L, H, T, d)).astype(np.float32)
+    k[0, 0, 2, 32 + 7] = np.inf
+    k[0, 0, 5, 96 + 30] = np.nan
+    k[0, 0, 6, 3] = -np.inf
+    kb = synth.f32_to_bf16_bits(k)
+    vb = synth.f32_to_bf16_bits(rng.standard_normal((L, H, T, d)).astype(np.float32))
+    pool = pk.Pool(L, H, d, T, "bf16")
+    pool.encode(_dev(torch, kb), _dev(torch, vb))
+    torch.cuda.synchronize()
+    ref = oracle.attention.encode_pool(kb, vb, "bf16", b32)
+    f = {n: x.cpu().numpy()[:, :, :T] for n, x in pool.fields().items()}
+    for (t, blk) in ((2, 1), (5, 3), (6, 0)):
+        assert not np.isfinite(ref["k_scales"][0, 0, t, blk]) and not np.isfinite(f["k_scales"][0, 0, t, blk])
+        assert np.isnan(ref["k_scales"][0, 0, t, blk]) == np.isnan(f["k_scales"][0, 0, t, blk])
+        assert np.all(f["k_codes"][0, 0, t, 32 * blk:32 * blk + 32] == 0)
+    fin = np.isfinite(ref["k_scales"])
+    assert np.array_equal(f["k_scales"][fin].view(np.uint16), ref["k_scales"][fin].view(np.uint16))
+    assert np.array_equal(f["k_codes"], ref["k_codes"])
+    assert np.array_equal(f["v_packed"], ref["v_packed"])
+    assert np.array_equal(f["v_norms"].view(np.uint16), ref["v_norms"].view(np.uint16))
+
+
 # ---- pool + private per-agent suffix under one softmax
 def run_suffix_case(env, L, H, Hq, d, T, A, S, dtype, seed=0, q_mult=1.0):
     pk, torch, c32, b32 = env
