@@ -1,6 +1,6 @@
 // Multi-agent decode attention over the shared pool on the 5th-generation
-// tensor cores (tcgen05, TMEM accumulators), head_dim 128, up to 64 query
-// rows per kv head (agents x GQA group).
+// tensor cores (tcgen05, TMEM accumulators), head_dim 128, any number of
+// query rows per kv head (agents x GQA group), taken in row groups of 64.
 //
 // PolyKV abstract ("PolyKV: A Shared Asymmetrically-Compressed KV Cache Pool
 // for Multi-Agent LLM Inference"): N agents read one compressed pool. With 15
@@ -29,19 +29,20 @@
 // one own tile ahead, into padded per-token rows. The ring's readers fence
 // the async proxy before releasing a stage (the TMA refill is an async-proxy
 // write after their generic loads). Every pool byte is read from HBM
-// once for all agents. The (layer, kv head, tile) list is cut into one
-// contiguous range per CTA (one persistent CTA per SM); a range that crosses a
-// unit boundary writes one softmax partial per unit piece; the merge kernel
-// combines them.
+// once for all agents of a row group. A segment is one (layer, kv head, row
+// group); the (segment, tile) list is cut into one contiguous range per CTA
+// (one persistent CTA per SM), a range that crosses a segment boundary writes
+// one softmax partial per segment piece, and the merge kernel combines them.
 //
-// Warp roles (576 threads): 0-7 producers in two groups of four warps that
+// Warp roles (832 threads): 0-7 producers in two groups of four warps that
 // take alternate tiles (each thread: one token's key codes -> exact hi/lo fp16
 // in TMEM, then its value codes -> norm-scaled centroids in shared memory),
-// 8-15 softmax in two row groups of 32, 16 MMA issue (an event loop over both
-// MMA chains) + TMEM owner, 17 TMA. Every mbarrier wait is bounded
-// (2 s); on expiry the CTA raises an abort flag, skips the rest of its work,
-// waits (bounded) for its copies in flight, frees its TMEM and sets the pool's
-// status word.
+// 8-23 softmax in four row groups of 16 (one warp per TMEM lane quadrant and
+// group), 24 MMA issue (an event loop over both MMA chains, run by the whole
+// warp with one elected lane issuing) + TMEM owner, 25 TMA. Every mbarrier
+// wait is bounded (2 s); on expiry the CTA raises an abort flag, skips the
+// rest of its work, waits (bounded) for its copies in flight, frees its TMEM
+// and sets the pool's status word.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
