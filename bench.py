@@ -139,6 +139,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ----------------------------------------------------------------------------- multi-rank helpers
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time: every rank gets the maximum of x over the process group."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank moves bytes_per_rank per step (weak scaling), and the step
+    takes the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, w: synth.Workload):
     """The CPU oracle, timed as it stands, on a bounded sample per step."""
@@ -307,11 +325,7 @@ def run_polykv(args, w: synth.Workload):
     e2e_ms_m = float(np.mean(e2e_ms)) if e2e_ms else float("nan")
 
     def allmax(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, world, dev)
 
     step_ms = allmax(step_ms)
     enc_ms_m = allmax(enc_ms_m)
@@ -321,7 +335,7 @@ def run_polykv(args, w: synth.Workload):
 
     enc_b, att_b = algorithmic_bytes(w, T, A)
     peak, peak_src = measured_peaks()
-    value = world * (enc_b + att_b) / (step_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, enc_b + att_b, step_ms)
     att_gbs = att_b / (att_alone_ms * 1e-3) / 1e9
     enc_gbs = enc_b / (enc_ms_m * 1e-3) / 1e9
     enc_tok_s = world * T / (enc_ms_m * 1e-3)
@@ -350,7 +364,7 @@ def run_polykv(args, w: synth.Workload):
                    "us": enc_ms_m * 1e3, "bytes": enc_b},
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs"},
-        "e2e": {"value": world * (enc_b + att_b) / (e2e_ms_m * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": whole_job_gbs(world, enc_b + att_b, e2e_ms_m), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_m},
         "gpu_launches": args.steps * (3 + (1 if w.suffix_len else 0)),
         "clocks": clocks,
