@@ -94,24 +94,30 @@ class ClockSampler:
         self.path = None
 
     def start(self):
-        try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
-                                         stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
-            return
-        # the timed region starts only once the sampler is live (its first row is written), so that
-        # its samples fall inside the region rather than after it
-        t_end = time.time() + 3.0
-        while time.time() < t_end and self.proc.poll() is None:
-            self.f.flush()
-            if os.path.getsize(self.path) > 0:
-                break
-            time.sleep(0.01)
+        # 20 ms sampling; if this nvidia-smi refuses that interval, the recipe's 200 ms
+        for period in ("20", "200"):
+            try:
+                fd, self.path = tempfile.mkstemp(suffix=".csv")
+                os.close(fd)
+                self.f = open(self.path, "w")
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                              "--format=csv,noheader,nounits", "-lms", period], stdout=self.f,
+                                             stderr=subprocess.DEVNULL)
+            except Exception:
+                self.proc = None
+                return
+            # the timed region starts only once the sampler is live (its first row is written), so
+            # that its samples fall inside the region rather than after it
+            t_end = time.time() + 3.0
+            while time.time() < t_end and self.proc.poll() is None:
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.01)
+            if self.proc.poll() is None or os.path.getsize(self.path) > 0:
+                return
+            self.f.close()
+            os.unlink(self.path)
+        self.proc = None
 
     def stop(self):
         if self.proc is None:
