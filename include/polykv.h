@@ -123,6 +123,9 @@ POLYKV_API polykv_status polykv_pool_get_regions(const polykv_pool* pool, polykv
  * The encode also raises the per-unit maximum of ||v|| kept in the pool header
  * (attention uses it to scale fp16 operands); the first encode into a pool
  * clears that header first (a cudaMemsetAsync on `stream`).
+ * Non-finite keys: a 32-element block holding an infinity or a NaN gets a
+ * non-finite scale and all-zero codes (attention over such a pool is
+ * undefined). Non-finite values are not supported.
  * Errors: E_INVAL, E_STATE (t0 beyond the encoded prefix), E_CUDA. */
 POLYKV_API polykv_status polykv_encode(polykv_pool* pool, const void* k, const void* v, int64_t t0, int64_t n_tokens,
                             void* stream);
