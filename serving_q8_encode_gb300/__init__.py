@@ -164,6 +164,20 @@ def polykv_codebook():
 
 
 # ------------------------------------------------------------------ torch wrapper
+def _require(t, name: str, *, shape=None, elem_bytes=None, dtype=None, device=None):
+    """Argument checks before a pointer crosses the C ABI (which sees only addresses and sizes)."""
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if elem_bytes is not None and t.element_size() != elem_bytes:
+        raise ValueError(f"{name} must have {elem_bytes}-byte elements (the pool dtype's bits), got {t.dtype}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the pool on {device}")
+
+
 def _stream_handle(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -203,9 +217,12 @@ class Pool:
 
     def encode(self, k, v, t0: int = 0, stream=None):
         """k, v: device tensors [L][H][n][d] (the pool's dtype, or int16/uint16 bits), contiguous."""
-        assert k.is_contiguous() and v.is_contiguous() and k.shape == v.shape
+        if k.dim() != 4:
+            raise ValueError(f"k must be [L][H][n][d], got shape {tuple(k.shape)}")
         L, H, n, d = k.shape
-        assert (L, H, d) == (self.desc.n_layers, self.desc.n_kv_heads, self.desc.head_dim)
+        want = (self.desc.n_layers, self.desc.n_kv_heads, n, self.desc.head_dim)
+        _require(k, "k", shape=want, elem_bytes=2, device=self.buf.device)
+        _require(v, "v", shape=want, elem_bytes=2, device=self.buf.device)
         polykv_encode(self.handle, k.data_ptr(), v.data_ptr(), t0, n, _stream_handle(stream))
 
     def status(self, stream=None) -> int:
@@ -217,15 +234,19 @@ class Pool:
     def attend(self, q, n_ctx: int, out=None, workspace=None, softmax_scale: float = 0.0, stream=None):
         """q: device [L][A][Hq][d] (pool dtype bits). Returns fp32 out of the same shape."""
         import torch
-        assert q.is_contiguous()
+        if q.dim() != 4:
+            raise ValueError(f"q must be [L][A][Hq][d], got shape {tuple(q.shape)}")
         L, A, Hq, d = q.shape
+        _require(q, "q", elem_bytes=2, device=self.buf.device)
         if out is None:
             out = torch.empty((L, A, Hq, d), dtype=torch.float32, device=q.device)
+        _require(out, "out", shape=(L, A, Hq, d), dtype=torch.float32, device=self.buf.device)
         need = self.workspace_size(A, Hq, n_ctx)
         if workspace is None:
             if self._ws is None or self._ws.numel() < need:
                 self._ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
             workspace = self._ws
+        _require(workspace, "workspace", device=self.buf.device)
         polykv_attend(self.handle, q.data_ptr(), out.data_ptr(), A, Hq, n_ctx, softmax_scale,
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
         return out
@@ -235,11 +256,17 @@ class Pool:
         """Pool plus each agent's private uncompressed suffix under one softmax.
         suffix_k/v: device [L][A][H][S][d] (pool dtype bits), contiguous."""
         import torch
+        if q.dim() != 4 or suffix_k.dim() != 5:
+            raise ValueError("q must be [L][A][Hq][d] and the suffix [L][A][H][S][d]")
         L, A, Hq, d = q.shape
-        assert suffix_k.is_contiguous() and suffix_v.is_contiguous() and suffix_k.shape == suffix_v.shape
+        _require(q, "q", elem_bytes=2, device=self.buf.device)
+        sfx_shape = (L, A, self.desc.n_kv_heads, suffix_k.shape[3], d)
+        _require(suffix_k, "suffix_k", shape=sfx_shape, elem_bytes=2, device=self.buf.device)
+        _require(suffix_v, "suffix_v", shape=sfx_shape, elem_bytes=2, device=self.buf.device)
         ext = AttendExt(suffix_k.data_ptr(), suffix_v.data_ptr(), suffix_k.shape[3])
         if out is None:
             out = torch.empty((L, A, Hq, d), dtype=torch.float32, device=q.device)
+        _require(out, "out", shape=(L, A, Hq, d), dtype=torch.float32, device=self.buf.device)
         need = polykv_attend_ex_workspace_size(self.handle, A, Hq, n_ctx, ext)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
         polykv_attend_ex(self.handle, q.data_ptr(), out.data_ptr(), A, Hq, n_ctx, softmax_scale, ext, ws.data_ptr(),
@@ -252,15 +279,21 @@ class Pool:
         bits, contiguous). Query token c of agent a sees the pool plus that agent's chunk tokens 0..c.
         Returns fp32 [L][A][C][Hq][d]."""
         import torch
+        if q.dim() != 5:
+            raise ValueError(f"q must be [L][A][C][Hq][d], got shape {tuple(q.shape)}")
         L, A, C, Hq, d = q.shape
-        assert q.is_contiguous() and chunk_k.is_contiguous() and chunk_v.is_contiguous()
-        assert chunk_k.shape == chunk_v.shape and chunk_k.shape[3] == C
+        _require(q, "q", elem_bytes=2, device=self.buf.device)
+        chunk_shape = (L, A, self.desc.n_kv_heads, C, d)
+        _require(chunk_k, "chunk_k", shape=chunk_shape, elem_bytes=2, device=self.buf.device)
+        _require(chunk_v, "chunk_v", shape=chunk_shape, elem_bytes=2, device=self.buf.device)
         ext = AttendExt(chunk_k=chunk_k.data_ptr(), chunk_v=chunk_v.data_ptr(), chunk_len=C)
         if out is None:
             out = torch.empty((L, A, C, Hq, d), dtype=torch.float32, device=q.device)
+        _require(out, "out", shape=(L, A, C, Hq, d), dtype=torch.float32, device=self.buf.device)
         need = polykv_attend_ex_workspace_size(self.handle, A, Hq, n_ctx, ext)
         if workspace is None:
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        _require(workspace, "workspace", device=self.buf.device)
         polykv_attend_ex(self.handle, q.data_ptr(), out.data_ptr(), A, Hq, n_ctx, softmax_scale, ext,
                          workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
         return out
