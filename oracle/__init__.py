@@ -15,12 +15,14 @@ Precision: the encode steps decide integers (codes), so they run in fp32 with
 a fixed operation order that the GPU kernels also follow; attention runs in
 float64 over the dequantized pool (the plain definition).
 
-Parity status per function (what pins it is in tests/test_oracle_pins.py):
+Parity status per function (what pins it is in tests/test_oracle_pins.py; each planted
+mistake there -- an FWHT sign, half-even rounding, the pack bit order, the GQA head mapping --
+turns a pin red):
   codebook.lloyd_max_normal     pinned (Max 1960 table, quadrature, sampled k-means)
   keys.quantize_q8_0            pinned (exact-rational brute force, round-trip bound)
   values.fwht_*                 pinned (scipy Hadamard matrix, self-inverse, norm)
   values.encode_values          pinned (nearest-centroid brute force, sum u^2 = d, NMSE)
-  values.pack_codes             pinned (hand-computed bytes, round trip)
+  values.pack_codes             pinned (hand-packed 32-token group, round trip, group independence)
   attention.attend              pinned (closed forms: q=0 mean, T=1, dominant key,
                                 constant V, two-token logistic, GQA mapping)
   accounting.*                  pinned (abstract's 2.91x, 97.7%, 0.45 GB)

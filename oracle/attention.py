@@ -33,6 +33,11 @@ def attend_rows(qrows: np.ndarray, khat: np.ndarray, vhat: np.ndarray, scale: fl
     return p @ vhat
 
 
+def kv_head_of(hq: int, G: int, H: int) -> int:
+    """The kv head read by query head hq (grouped-query attention: G query heads per kv head)."""
+    return hq // G
+
+
 def attend_layer(q_l: np.ndarray, khat_l: np.ndarray, vhat_l: np.ndarray, scale: float,
                  suffix_k=None, suffix_v=None) -> np.ndarray:
     """q_l [A][Hq][d]; khat_l, vhat_l [H][T][d]; optional private per-agent
@@ -44,7 +49,7 @@ def attend_layer(q_l: np.ndarray, khat_l: np.ndarray, vhat_l: np.ndarray, scale:
     out = np.zeros((A, Hq, d), dtype=np.float64)
     for a in range(A):
         for hq in range(Hq):
-            h = hq // G
+            h = kv_head_of(hq, G, H)
             kk, vv = khat_l[h], vhat_l[h]
             if suffix_k is not None:
                 kk = np.concatenate([kk, suffix_k[a, h]], axis=0)
@@ -65,7 +70,7 @@ def attend_chunk_layer(q_l: np.ndarray, khat_l: np.ndarray, vhat_l: np.ndarray, 
     out = np.zeros((A, C, Hq, d), dtype=np.float64)
     for a in range(A):
         for hq in range(Hq):
-            h = hq // G
+            h = kv_head_of(hq, G, H)
             kk = np.concatenate([khat_l[h], chunk_k[a, :, h]], axis=0)
             vv = np.concatenate([vhat_l[h], chunk_v[a, :, h]], axis=0)
             lim = T + 1 + np.arange(C)
@@ -117,11 +122,15 @@ def attend_pool(q_bits, dtype, pool, n_ctx, centroids_f32, scale=None, layers=No
 
 def encode_pool(k_bits, v_bits, dtype, boundaries_f32):
     """Oracle encode of K/V bit patterns [L][H][T][d] -> unpacked pool dict
-    (plus packed codes and the pre-quantization u for boundary checks)."""
+    (plus the packed codes [L][H][ceil(T/32)][d][12] and the pre-quantization u
+    for boundary checks)."""
     k = _keys.bits_to_f32(k_bits, dtype)
     kc, ks = _keys.quantize_q8_0(k)
     del k
     v = _keys.bits_to_f32(v_bits, dtype)
     vc, vn, u = _values.encode_values(v, boundaries_f32)
+    T = vc.shape[-2]
+    pad = (-T) % _values.GROUP   # a partly filled last group: its missing tokens packed as code 0
+    vpad = np.concatenate([vc, np.zeros(vc.shape[:-2] + (pad, vc.shape[-1]), np.uint8)], axis=-2) if pad else vc
     return {"k_codes": kc, "k_scales": ks, "v_codes": vc, "v_norms": vn,
-            "v_packed": _values.pack_codes(vc), "u": u}
+            "v_packed": _values.pack_codes(vpad), "u": u}

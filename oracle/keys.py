@@ -30,6 +30,11 @@ def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
     return bf16_bits_to_f32(bits) if dtype == "bf16" else f16_bits_to_f32(bits)
 
 
+def round_half_away(r64: np.ndarray) -> np.ndarray:
+    """Nearest integer, ties away from zero (q8_0's rounding), exact in float64."""
+    return np.sign(r64) * np.floor(np.abs(r64) + 0.5)
+
+
 def quantize_q8_0(x: np.ndarray):
     """x: fp32 [..., d] (d a multiple of 32). Returns (codes int8 [..., d], scales fp16 [..., d/32])."""
     x = np.asarray(x, dtype=np.float32)
@@ -43,10 +48,7 @@ def quantize_q8_0(x: np.ndarray):
     usable = (sf > 0) & np.isfinite(sf)
     safe = np.where(usable, sf, np.float32(1.0))[..., None]
     r = (xb / safe).astype(np.float32)                          # correctly rounded fp32 quotient
-    # round half away from zero, evaluated exactly in float64
-    r64 = r.astype(np.float64)
-    q = np.sign(r64) * np.floor(np.abs(r64) + 0.5)
-    q = np.clip(q, -127, 127)
+    q = np.clip(round_half_away(r.astype(np.float64)), -127, 127)
     q = np.where(usable[..., None], q, 0.0)
     return q.astype(np.int8).reshape(x.shape), s16
 

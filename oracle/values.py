@@ -19,8 +19,11 @@ Readings taken (the abstract is silent on them):
         (a, b) -> (a + b, a - b) with a the lower index;
       - u_j = y_j / ||v|| correctly rounded; u = 0 when ||v|| = 0;
   * code_j = #{i : u_j >= b_i} over the 7 fp32 boundaries (ties go up);
-  * 8 codes per 3 bytes: coordinate 8g+i sits at bits 3i..3i+2 of a
-    little-endian 24-bit word (d=128 -> 48 bytes, d=64 -> 24 bytes);
+  * packing (3 bits per code, no padding): the pool keeps codes in groups of
+    32 consecutive tokens of one (layer, kv head); for each coordinate j the
+    group's 32 codes form one little-endian 96-bit (12-byte) string, token k
+    of the group at bits 3k..3k+2, and the d strings of a group follow in
+    coordinate order (12*d bytes per 32 tokens = 3d/8 bytes per token);
   * the stored norm is fp16 (round to nearest even); the codes use the
     unrounded fp32 norm.
 Dequantized value: v_hat = H_n((n16 / sqrt(d)) * C[code]) = (n16 / d) * H C[code].
@@ -28,6 +31,11 @@ Dequantized value: v_hat = H_n((n16 / sqrt(d)) * C[code]) = (n16 / d) * H C[code
 from __future__ import annotations
 
 import numpy as np
+
+
+def butterfly(a, b):
+    """One Walsh-Hadamard butterfly: (a, b) -> (a + b, a - b), a the lower index."""
+    return a + b, a - b
 
 
 def fwht_f32_pinned(v: np.ndarray) -> np.ndarray:
@@ -38,9 +46,7 @@ def fwht_f32_pinned(v: np.ndarray) -> np.ndarray:
     h = 1
     while h < d:
         y = y.reshape(lead + (d // (2 * h), 2, h))
-        a = y[..., 0, :]
-        b = y[..., 1, :]
-        y = np.stack([a + b, a - b], axis=-2).astype(np.float32)
+        y = np.stack(butterfly(y[..., 0, :], y[..., 1, :]), axis=-2).astype(np.float32)
         h *= 2
     return y.reshape(lead + (d,))
 
@@ -53,9 +59,7 @@ def fwht_f64(v: np.ndarray) -> np.ndarray:
     h = 1
     while h < d:
         y = y.reshape(lead + (d // (2 * h), 2, h))
-        a = y[..., 0, :]
-        b = y[..., 1, :]
-        y = np.stack([a + b, a - b], axis=-2)
+        y = np.stack(butterfly(y[..., 0, :], y[..., 1, :]), axis=-2)
         h *= 2
     return y.reshape(lead + (d,))
 
@@ -94,23 +98,30 @@ def encode_values(v: np.ndarray, boundaries_f32: np.ndarray):
     return codes, n.astype(np.float16), u
 
 
+GROUP = 32  # tokens per packed code group
+
+
 def pack_codes(codes: np.ndarray) -> np.ndarray:
-    """uint8 codes [..., d] -> packed bytes [..., 3d/8]."""
-    c = np.asarray(codes, dtype=np.uint32)
-    d = c.shape[-1]
-    g = c.reshape(c.shape[:-1] + (d // 8, 8))
-    w = np.zeros(g.shape[:-1], dtype=np.uint32)
-    for i in range(8):
-        w |= g[..., i] << np.uint32(3 * i)
-    out = np.stack([w & 0xFF, (w >> 8) & 0xFF, (w >> 16) & 0xFF], axis=-1).astype(np.uint8)
-    return out.reshape(c.shape[:-1] + (3 * d // 8,))
+    """uint8 codes [..., T, d] (T a multiple of 32) -> packed bytes [..., T/32, d, 12]:
+    string (group, j) holds token k of the group at bits 3k..3k+2 (little endian)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    T, d = c.shape[-2], c.shape[-1]
+    assert T % GROUP == 0, "pack_codes takes whole 32-token groups"
+    g = c.reshape(c.shape[:-2] + (T // GROUP, GROUP, d))
+    g = np.swapaxes(g, -1, -2)                                   # [..., G, d, 32 tokens]
+    bits = np.stack([(g >> b) & 1 for b in range(3)], axis=-1)   # [..., G, d, 32, 3]: bit 3k+b
+    bits = bits.reshape(bits.shape[:-2] + (3 * GROUP,)).astype(np.uint8)
+    return np.packbits(bits, axis=-1, bitorder="little")         # [..., G, d, 12]
 
 
 def unpack_codes(packed: np.ndarray, d: int) -> np.ndarray:
-    p = np.asarray(packed, dtype=np.uint32).reshape(packed.shape[:-1] + (d // 8, 3))
-    w = p[..., 0] | (p[..., 1] << np.uint32(8)) | (p[..., 2] << np.uint32(16))
-    out = np.stack([(w >> np.uint32(3 * i)) & 7 for i in range(8)], axis=-1).astype(np.uint8)
-    return out.reshape(packed.shape[:-1] + (d,))
+    """packed bytes [..., G, d, 12] -> uint8 codes [..., 32*G, d]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    assert p.shape[-2] == d and p.shape[-1] == 3 * GROUP // 8
+    bits = np.unpackbits(p, axis=-1, bitorder="little").reshape(p.shape[:-1] + (GROUP, 3))
+    codes = (bits[..., 0] | (bits[..., 1] << 1) | (bits[..., 2] << 2)).astype(np.uint8)   # [..., G, d, 32]
+    codes = np.swapaxes(codes, -1, -2)                                                      # [..., G, 32, d]
+    return codes.reshape(codes.shape[:-3] + (codes.shape[-3] * GROUP, d))
 
 
 def dequantize_values(codes: np.ndarray, norm16: np.ndarray, centroids_f32: np.ndarray) -> np.ndarray:

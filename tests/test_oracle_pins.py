@@ -234,16 +234,36 @@ def test_zero_value_vector():
     assert np.all(values.dequantize_values(codes, n16, c32) == 0)
 
 
+def _check_pack_worked_group():
+    rows = {r[0]: r[1:] for r in _read_golden("pack_worked_group.txt")}
+    c0 = np.array([int(x) for x in rows["codes0"]], np.uint8)
+    c1 = np.array([int(x) for x in rows["codes1"]], np.uint8)
+    want = np.array([int(x, 16) for x in rows["bytes"]], np.uint8).reshape(2, 12)
+    got = values.pack_codes(np.stack([c0, c1], axis=-1))      # [32 tokens][2 coordinates]
+    assert got.shape == (1, 2, 12)
+    assert np.array_equal(got[0], want)
+
+
 def test_pack_worked_group_and_roundtrip():
-    rows = _read_golden("pack_worked_group.txt")
-    codes = np.array([int(x) for x in rows[0][1:]], np.uint8)
-    want = np.array([int(x, 16) for x in rows[1][1:]], np.uint8)
-    assert np.array_equal(values.pack_codes(codes[None, :])[0], want)
+    _check_pack_worked_group()
     rng = np.random.default_rng(9)
-    c = rng.integers(0, 8, (77, 128)).astype(np.uint8)
+    c = rng.integers(0, 8, (3, 96, 128)).astype(np.uint8)
     p = values.pack_codes(c)
-    assert p.shape == (77, 48)
+    assert p.shape == (3, 3, 128, 12)                          # 3 bits per code: 12 bytes per 32 tokens
     assert np.array_equal(values.unpack_codes(p, 128), c)
+
+
+def test_pack_group_independence():
+    """Each 12-byte string depends only on its own coordinate and 32-token group."""
+    rng = np.random.default_rng(4)
+    c = rng.integers(0, 8, (64, 16)).astype(np.uint8)
+    p = values.pack_codes(c)
+    c2 = c.copy()
+    c2[40, 5] ^= 7                                             # token 40 = group 1, k = 8
+    p2 = values.pack_codes(c2)
+    diff = np.argwhere(p != p2)
+    assert set(map(tuple, diff[:, :2])) == {(1, 5)}
+    assert set(diff[:, 2]) == {3}                              # bits 24..26 live in byte 3
 
 
 # ---------------------------------------------------------------- attention
@@ -377,29 +397,34 @@ def test_exact_ratio_with_overheads():
 
 
 # ---------------------------------------------------------------- planted mistakes
+# Each test plants a plausible mistake inside the oracle (monkeypatching one of its steps) and
+# checks that a pin above goes red; the pins then pass again with the oracle restored.
 def test_planted_fwht_sign_error_is_caught(monkeypatch):
-    def bad(v):
-        y = np.array(v, dtype=np.float64, copy=True)
-        d = y.shape[-1]
-        h = 1
-        while h < d:
-            y = y.reshape(y.shape[:-1] if False else (-1, d // (2 * h), 2, h))
-            a, b = y[..., 0, :], y[..., 1, :]
-            y = np.stack([a + b, b - a], axis=-2).reshape(-1, d)
-            h *= 2
-        return y
-    rng = np.random.default_rng(1)
-    v = rng.standard_normal((4, 64))
-    y = bad(v) / 8.0
-    assert not np.allclose(bad(y) / 8.0, v, atol=1e-6)
+    monkeypatch.setattr(values, "butterfly", lambda a, b: (a + b, b - a))
+    with pytest.raises(AssertionError):
+        test_fwht_matches_scipy_hadamard(64)
+    with pytest.raises(AssertionError):
+        test_value_nmse_gaussian_d128()
 
 
-def test_planted_half_even_rounding_is_caught():
-    rows = _read_golden("q8_0_worked_block.txt")
-    x = np.array([float(r[0]) for r in rows], np.float64)
-    want = np.array([int(r[2]) for r in rows])
-    half_even = np.round(x / 0.0625).astype(int)
-    assert not np.array_equal(half_even, want)
+def test_planted_half_even_rounding_is_caught(monkeypatch):
+    monkeypatch.setattr(keys, "round_half_away", np.round)   # numpy rounds ties to even
+    with pytest.raises(AssertionError):
+        test_q8_worked_block()
+
+
+def test_planted_pack_bit_order_is_caught(monkeypatch):
+    real = np.packbits
+    monkeypatch.setattr(values.np, "packbits", lambda a, axis=-1, bitorder="little": real(a, axis=axis, bitorder="big"))
+    with pytest.raises(AssertionError):
+        _check_pack_worked_group()
+
+
+def test_planted_gqa_mapping_is_caught(monkeypatch):
+    """A query head reading kv head hq % H instead of hq // G fails the GQA pin."""
+    monkeypatch.setattr(attention, "kv_head_of", lambda hq, G, H: hq % H)
+    with pytest.raises(AssertionError):
+        test_attention_gqa_head_mapping()
 
 
 def test_q8_subnormal_scale_clamp_binds():
