@@ -67,8 +67,10 @@ typedef struct {
  * unit u = layer * n_kv_heads + kv_head, token t:
  *   k_codes  int8    [U][C][head_dim]        at k_codes_off + (u*C + t)*head_dim
  *   k_scales fp16    [U][C][head_dim/32]     at k_scales_off + 2*((u*C + t)*head_dim/32 + block)
- *   v_codes  uint8   [U][C][3*head_dim/8]    8 codes per 3 bytes: coordinate 8g+i at bits 3i..3i+2
- *                                            of the little-endian 24-bit word of group g
+ *   v_codes  uint8   [U][C/32][head_dim][12] per group of 32 consecutive tokens and coordinate j,
+ *                                            one little-endian 96-bit string holding the 3-bit codes
+ *                                            of the group's tokens, token t at bits 3(t%32)..3(t%32)+2
+ *                                            (3 bits per code, 3*head_dim/8 bytes per token)
  *   v_norms  fp16    [U][C]                  ||v|| of the unrotated value vector
  */
 typedef struct {

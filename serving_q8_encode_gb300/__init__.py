@@ -307,6 +307,7 @@ class Pool:
         b = self.buf
         kq = b[r.k_codes_off:r.k_codes_off + L * H * C * d].view(torch.int8).view(L, H, C, d)
         ks = b[r.k_scales_off:r.k_scales_off + L * H * C * (d // 32) * 2].view(torch.float16).view(L, H, C, d // 32)
-        vc = b[r.v_codes_off:r.v_codes_off + L * H * C * (3 * d // 8)].view(L, H, C, 3 * d // 8)
+        # value codes: per 32-token group and coordinate one 12-byte string (token k at bits 3k..3k+2)
+        vc = b[r.v_codes_off:r.v_codes_off + L * H * C * (3 * d // 8)].view(L, H, C // 32, d, 12)
         vn = b[r.v_norms_off:r.v_norms_off + L * H * C * 2].view(torch.float16).view(L, H, C)
         return {"k_codes": kq, "k_scales": ks, "v_packed": vc, "v_norms": vn}

@@ -9,7 +9,7 @@
 // split for all agents. Keys are dequantized in registers (int8 code times
 // the block's fp16 scale, applied to the 32-wide partial dot product); the
 // online softmax runs in base 2; values are accumulated in the ROTATED basis
-// as p * ||v|| * centroid[code]. Because the inverse transform is linear, the
+// as (p * ||v||) * centroid[code]. Because the inverse transform is linear, the
 // merge kernel applies one inverse FWHT per output row instead of one per
 // value vector:  o = (1/d) H (sum_t p_t n_t C[code_t]) / sum_t p_t.
 #include <algorithm>
@@ -40,7 +40,7 @@ struct SimtSmem {
     static constexpr int kQs = D * RMAX;            // [D][RMAX]
     static constexpr int kSc = RMAX * (kTT + 1);    // [RMAX][kTT+1]
     static constexpr int kVh = kTT * (D + 4);       // [kTT][D+4]
-    static constexpr int kFloats = kQs + kSc + kVh + 3 * RMAX;
+    static constexpr int kFloats = kQs + kSc + kVh + 3 * RMAX + kTT;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
     float* m_s = vh + S::kVh;
     float* l_s = m_s + RMAX;
     float* al_s = l_s + RMAX;
+    float* nvs = al_s + RMAX;         // [kTT] norms of the tile's tokens (0 past the split)
 
     const int tid = threadIdx.x;
     const int split = blockIdx.x;
@@ -149,43 +150,27 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
                 if (r < nrows) sc[r * (kTT + 1) + t] = valid ? score[i] * scale_log2 : -INFINITY;
             }
         }
-        // ---- C: dequantize the value tile to n * centroid[code] (rotated basis)
+        // ---- C: centroids of the value tile in the rotated basis, vh[t][j] = C[code]; each token's
+        // norm is applied to its probability in B. The tile (64 tokens, 64-aligned) is two 32-token
+        // groups of the pool, one 12-byte string per (group, coordinate).
         {
-            const int t = tid / 2, half = tid % 2;
-            const int64_t tok = tile + t;
-            const bool valid = tok < t_end;
-            float* dst = vh + t * (D + 4) + half * (D / 2);
-            if (valid) {
-                const float nv = __half2float(p.vn[ubase + tok]);
-                const uint32_t* cw =
-                    reinterpret_cast<const uint32_t*>(p.vc + (ubase + tok) * (3 * D / 8) + half * (3 * D / 16));
-                constexpr int NW = 3 * D / 64;   // 32-bit words per half row
-                uint32_t w[NW];
+            if (tid < kTT) {
+                const int64_t tok = tile + tid;
+                nvs[tid] = tok < t_end ? __half2float(p.vn[ubase + tok]) : 0.0f;
+            }
+            const int64_t gbase = (ubase + tile) / 32;
+            for (int it = tid; it < 2 * D; it += kThreads) {
+                const int h = it / D, j = it % D;
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(p.vc + ((gbase + h) * D + j) * 12);
+                const uint32_t w[3] = {src[0], src[1], src[2]};
+                float* col = vh + (32 * h) * (D + 4) + j;
 #pragma unroll
-                for (int i = 0; i < NW; ++i) w[i] = cw[i];
-#pragma unroll
-                for (int g8 = 0; g8 < D / 16; ++g8) {  // 8-code groups in this half
-                    // bytes 3*g8 .. 3*g8+2 of the half row
-                    uint32_t w24 = 0;
-#pragma unroll
-                    for (int bb = 0; bb < 3; ++bb) {
-                        const int byte = 3 * g8 + bb;
-                        w24 |= ((w[byte >> 2] >> (8 * (byte & 3))) & 0xFF) << (8 * bb);
-                    }
-                    float4 lo, hi;
-                    lo.x = nv * centroid_signed((w24 >> 0) & 7);
-                    lo.y = nv * centroid_signed((w24 >> 3) & 7);
-                    lo.z = nv * centroid_signed((w24 >> 6) & 7);
-                    lo.w = nv * centroid_signed((w24 >> 9) & 7);
-                    hi.x = nv * centroid_signed((w24 >> 12) & 7);
-                    hi.y = nv * centroid_signed((w24 >> 15) & 7);
-                    hi.z = nv * centroid_signed((w24 >> 18) & 7);
-                    hi.w = nv * centroid_signed((w24 >> 21) & 7);
-                    reinterpret_cast<float4*>(dst)[2 * g8] = lo;
-                    reinterpret_cast<float4*>(dst)[2 * g8 + 1] = hi;
+                for (int k = 0; k < 32; ++k) {
+                    const int bit = 3 * k, wi = bit >> 5, off = bit & 31;
+                    uint32_t c = w[wi] >> off;
+                    if (off > 29) c |= w[wi + 1] << (32 - off);
+                    col[k * (D + 4)] = centroid_signed(c & 7u);
                 }
-            } else {
-                for (int i = 0; i < D / 8; ++i) reinterpret_cast<float4*>(dst)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         __syncthreads();
@@ -209,8 +194,8 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
                 float sum = p0 + p1;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                row[lane] = p0;
-                row[lane + 32] = p1;
+                row[lane] = p0 * nvs[lane];   // the value operand carries no norm (see C)
+                row[lane + 32] = p1 * nvs[lane + 32];
                 if (lane == 0) {
                     l_s[r] = l_s[r] * alpha + sum;
                     m_s[r] = m_new;

@@ -5,47 +5,66 @@
 // PolyKV abstract ("PolyKV: A Shared Asymmetrically-Compressed KV Cache Pool
 // for Multi-Agent LLM Inference"): N agents read one compressed pool. With 15
 // agents x 4 GQA heads = 60 rows per kv head, q.K and p.V are dense
-// contractions (about 156 flop per pool byte), so both run as tcgen05.mma:
+// contractions, so both run as tcgen05.mma with every operand that changes per
+// token held in TMEM:
 //
-//   MMA1 (per 128-token tile): S^T[token][row] = K_hat[token][128] . Q'[row][128]^T
-//        with K_hat = s_b * code * 2^-4 split exactly into two fp16 halves
-//        (hi = fp16(K_hat), lo = K_hat - hi; the product has at most 18
-//        significant bits, so hi + lo = K_hat) held in TMEM as the A operand,
-//        and Q' the rows' queries in fp16 scaled by a power of two (bf16
-//        queries are then exact). One fp32 accumulator sums hi then lo.
+//   MMA1, per 128-token tile and q8_0 block b (dims 32b .. 32b+31):
+//        S_b^T[token][row] = Kc[token][32 dims] . Q'[row][32 dims]^T
+//        with Kc the int8 codes as exact fp16 (A operand in TMEM) and Q' the
+//        rows' queries in fp16 scaled by a power of two per row group (bf16
+//        queries are then exact); four fp32 accumulators, one per block.
 //   softmax (one thread per token and row group; TMEM lane = token):
-//        d = c * S - m (base-2 logits relative to the running max), lazy
-//        rescaling only when some d exceeds 2^8 (decided for the whole row
-//        group with one OR-reducing barrier), p = 2^d stored as fp16.
-//   MMA2: O^T[dim][row] += Vn[token][dim]^T . P[token][row], where
-//        Vn = centroid(code) * ||v|| * w in fp16 (w a power of two from the
-//        pool's per-unit norm maximum, so ||v|| w < 2^8): the value operand
-//        carries its norm, in the ROTATED basis; the merge kernel applies the
-//        inverse FWHT once per output row.
+//        d = sum_b c_b[token] S_b - m with c_b = (block scale) x (logit scale)
+//        / (query scale), i.e. the q8_0 scales are applied to the exact
+//        per-block dot products; base-2 logits relative to the running max,
+//        lazy rescaling only when some d exceeds 2^8 (decided per row group
+//        with one OR-reducing barrier); P' = 2^d * ||v|| * w stored as fp16
+//        (w a power of two from the pool's per-unit norm maximum, so
+//        ||v|| w < 2^7 and P' < 2^15).
+//   MMA2: O^T[dim][row] += Cv[dim][token] . P'[token][row]^T, Cv the
+//        centroids of the value codes in fp16 (A operand in TMEM, lane =
+//        dim), in the ROTATED basis; the merge kernel applies the inverse FWHT
+//        once per output row.
 //
-// Data movement: one TMA thread streams each tile's block scales, value codes
-// and norms (7.25 KB) into a 4-deep shared-memory ring; the key-code rows
-// (16 KB per tile) are copied by the producer warps themselves with cp.async,
-// one own tile ahead, into padded per-token rows. The ring's readers fence
-// the async proxy before releasing a stage (the TMA refill is an async-proxy
-// write after their generic loads). Every pool byte is read from HBM
-// once for all agents of a row group. A segment is one (layer, kv head, row
-// group); the (segment, tile) list is cut into one contiguous range per CTA
-// (one persistent CTA per SM), a range that crosses a segment boundary writes
-// one softmax partial per segment piece, and the merge kernel combines them.
+// The pool's value codes are stored per 32-token group and coordinate (one
+// 12-byte string each), so the thread owning TMEM lane j reads the 12 bytes of
+// coordinate j for its 32 tokens and writes their centroid pairs straight into
+// its lane: neither MMA operand built per tile passes through shared memory.
 //
-// Warp roles (832 threads): 0-7 producers in two groups of four warps that
-// take alternate tiles (each thread: one token's key codes -> exact hi/lo fp16
-// in TMEM, then its value codes -> norm-scaled centroids in shared memory),
-// 8-23 softmax in four row groups of 16 (one warp per TMEM lane quadrant and
-// group), 24 MMA issue (an event loop over both MMA chains, run by the whole
-// warp with one elected lane issuing) + TMEM owner, 25 TMA. Every mbarrier
-// wait is bounded (2 s); on expiry the CTA raises an abort flag, skips the
-// rest of its work, waits (bounded) for its copies in flight, frees its TMEM
-// and sets the pool's status word.
+// Data movement: one producer thread streams each tile's key codes (a 2-D
+// tensor copy with the 128-byte swizzle, so that every thread's 32-byte key
+// block reads conflict-free), value codes, block scales and norms (1-D bulk
+// copies) into a 5-stage shared-memory ring. Shared memory also holds the
+// queries and P' (the B operands) and a lane-replicated table of centroid
+// pairs. Each tile's eight MMA1 and eight MMA2 instructions are issued from one
+// asm statement each by an elected lane, with descriptors built once: the
+// issuing thread's instruction count, not the tensor core, bounds how fast
+// small-N MMAs go.
+//
+// Work split: one persistent CTA per SM. A segment is one (kv-head unit, row
+// group of up to 64 query rows); the (segment, tile) list is cut into one
+// contiguous range per CTA, a range that crosses a segment boundary writes one
+// softmax partial per segment piece (slot = segment + CTA), and the merge
+// kernel combines them. Every pool byte is read from HBM once per row group.
+//
+// Warp roles (640 threads): warps 0-15 are uniform workers, warp w owning row
+// group g = w / 4 (rows 16g .. 16g+15), q8_0 block g, token quarter g and TMEM
+// lane quadrant w % 4. Per tile each worker thread converts one 32-code key
+// block of its token (lane) into the next tile's key operand, runs the softmax
+// of its token for its 16 rows, and converts its coordinate's 32 value codes
+// into the value operand. Warp 16 issues the MMAs and owns the TMEM, warp 17
+// is the producer and warps 18-19 complete their warpgroup, whose registers go
+// to the workers (setmaxnreg). Every mbarrier wait is bounded (2 s); on expiry
+// the CTA raises an abort flag, runs its loops to the end with every wait
+// returning at once (so named barriers stay matched), waits (bounded) for its
+// copies and MMAs, frees its TMEM and sets the pool's status word.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "polykv_internal.cuh"
 #include "tc_ptx.cuh"
@@ -55,49 +74,52 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kD = 128;
-constexpr int kNR = 64;            // padded rows (MMA N)
-constexpr int kGroups = 4;                       // softmax row groups
-constexpr int kGRows = kNR / kGroups;            // 16 query rows per group
-constexpr int kSmWarps = 4 * kGroups;            // softmax warps (one per TMEM lane quadrant and group)
-constexpr int kSmThreads = 32 * kSmWarps;
-constexpr int kWarpMma = 8 + kSmWarps;           // MMA issue + TMEM owner
-constexpr int kWarpTma = kWarpMma + 1;
-constexpr int kThreadsTc = 32 * (kWarpTma + 1);  // 26 warps
-// named barriers: 1..4 sync one row group, 5..8 OR-reduce within one (never mixed on an id), 9 all softmax
-constexpr uint32_t kBarGroup = 1, kBarRed = 5, kBarSoftmax = 9;
-constexpr int kNS = 4;             // ring depth: scales / value codes / norms
-constexpr int kKS = 4;             // key-row stages: two per producer group (cp.async, one own tile ahead)
+constexpr int kNR = 64;            // padded rows per segment (MMA N)
+constexpr int kGroups = 4;         // row groups = q8_0 blocks = 32-token quarters
+constexpr int kGRows = kNR / kGroups;
+constexpr int kWorkers = 16;       // worker warps
+constexpr int kWarpMma = kWorkers;       // MMA issuer and TMEM owner
+constexpr int kWarpTma = kWorkers + 1;   // pool-tile producer
+constexpr int kThreadsTc = 32 * (kWorkers + 4);   // + one warpgroup: the MMA warp and three idle warps
+constexpr int kRegWorker = 104;    // registers per worker thread after setmaxnreg (launch: 96)
+// setmaxnreg draws on the registers the CTA was launched with: 640 x 96 = 61440 >= 512 x 104 + 128 x 56
+constexpr int kRegOther = 56;      // the MMA warpgroup's registers after setmaxnreg  // pool tiles prefetched into L2 ahead of MMA1
+// named barriers: 1..4 sync one row group, 5..8 OR-reduce within one (never mixed on an id)
+constexpr uint32_t kBarGroup = 1, kBarRed = 5;
 constexpr float kTau = 8.0f;       // lazy rescale threshold (log2 units): p <= 2^8
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kLog2eTc = 1.4426950408889634f;
 
-// one ring stage: block scales | value codes | norms
-constexpr uint32_t kRawS = 0, kRawV = 1024, kRawN = 7168;
-constexpr uint32_t kRawBytes = 7424;       // bytes delivered per tile
-constexpr uint32_t kRawStage = 7424;
-constexpr uint32_t kKRow = 144;            // padded key row: 8-lane phases of 16-byte loads hit distinct banks
-constexpr uint32_t kKStage = kTile * kKRow;
-
-// shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kSmQ = 0;                            // 2 chunks x [64 rows][128 B]             16 KB
-constexpr uint32_t kSmV = kSmQ + 16384;                 // 2 stages x 2 dim blocks x [128][128 B]  64 KB
-constexpr uint32_t kSmP = kSmV + 65536;                 // 2 stages x [128 tokens][128 B]          32 KB
-constexpr uint32_t kSmRaw = kSmP + 32768;               // kNS x 7.25 KB                           29 KB
-constexpr uint32_t kSmK = kSmRaw + kNS * kRawStage;     // kKS x 128 x 144 B                       72 KB
-constexpr uint32_t kSmLut = kSmK + kKS * kKStage;       // 64 code pairs x 32 lanes x 4 B            8 KB
+// shared memory map (bytes from an 8 KB-aligned base)
+constexpr int kStages = 5;                    // pool-tile ring depth
+constexpr uint32_t kStKeys = 0;               // stage: key codes [128 tokens][128 B], 128-byte swizzle  16 KB
+constexpr uint32_t kStVals = 16384;           //        value codes, 4 groups x 128 dims x 12 B           6 KB
+constexpr uint32_t kStScales = 22528;         //        block scales [128 tokens][4] fp16                 1 KB
+constexpr uint32_t kStNorms = 23552;          //        norms [128 tokens] fp16                            256 B
+constexpr uint32_t kStageTx = 23808;          // bytes the TMA delivers per stage
+constexpr uint32_t kStageBytes = 24576;       // stage stride (keys stay 1024-byte aligned)
+constexpr uint32_t kSmRing = 0;
+constexpr uint32_t kSmQ = kSmRing + kStages * kStageBytes;   // 2 buffers x 2 chunks x [64 rows][128 B]  32 KB
+constexpr uint32_t kSmP = kSmQ + 32768;       // 2 buffers x [128 tokens][128 B]                          32 KB
+constexpr uint32_t kSmLut = kSmP + 32768;     // 64 code pairs x 32 lanes x 4 B                            8 KB
 constexpr uint32_t kSmMisc = kSmLut + 8192;
-constexpr uint32_t kSmBytes = kSmMisc + 3072 + 1024;    // + alignment slack
+constexpr uint32_t kMiscBytes = 4096;
+constexpr uint32_t kSmBytes = kSmMisc + kMiscBytes + 8192;   // + alignment slack
 static_assert(kSmBytes <= 232448, "shared memory budget");
-static_assert(kSmK % 16 == 0 && kKRow % 16 == 0, "cp.async destinations are 16-byte aligned");
+static_assert(kSmLut % 8192 == 0 && kSmQ % 1024 == 0 && kSmP % 1024 == 0 && kStageBytes % 1024 == 0,
+              "alignment of the swizzled operands and of the OR-addressed table");
+static_assert(kThreadsTc / 32 == kWorkers + 4 && kWorkers % 4 == 0, "workers fill whole warpgroups");
+static_assert(kWorkers * 32 * kRegWorker + 128 * kRegOther <= kThreadsTc * 96, "setmaxnreg split");
 
 // TMEM columns
-constexpr uint32_t kColK = 0;     // 2 stages x (64 hi + 64 lo)
-constexpr uint32_t kColS = 256;   // 2 buffers x 64
-constexpr uint32_t kColO = 384;   // 64
-constexpr uint32_t kColL = 448;   // 64: per-token-slot partial row sums (lane = token slot)
+constexpr uint32_t kColS = 0;      // 4 blocks x 64 rows: S_b^T, lane = token
+constexpr uint32_t kColK = 256;    // 2 buffers x 64: key codes (fp16 pairs), lane = token
+constexpr uint32_t kColV = 384;    // 64: value centroids (fp16 pairs of tokens), lane = dim
+constexpr uint32_t kColO = 448;    // 64: O^T, lane = dim
 constexpr uint32_t kTmemCols = 512;
 
 struct TcParams {
+    CUtensorMap kmap;   // key codes as a 2-D tensor [U * cap rows][128 B], 128-byte swizzle, 128 x 128 boxes
     PoolView p;
     const uint16_t* q;
     float* ws_acc;
@@ -110,27 +132,25 @@ struct TcParams {
     int RS;      // rows per partial slot (64 with several row groups, else Rtot)
     int nt;      // tiles per segment (= per unit)
     int nctas;
-    int test_stall;  // test hook: the MMA thread issues nothing, so the softmax waits run out
+    int test_stall;  // test hook: the MMA thread issues nothing, so the workers' waits run out
     float scale_log2;
 };
 
 struct Misc {
-    float m[kNR];         // running max per row (log2 units); +inf for padding rows
-    float nm[kNR];        // -m
-    float alpha[kNR];     // 2^(m_old - m_new)
-    float red[kGroups][4][kGRows];   // per (group, lane quadrant, row): partial maxima or row sums
-    float qred[kSmWarps];
-    float scale_eff;
-    float wscale;
+    float m[kNR];                      // running max per row (log2 units); +inf for padding rows
+    float nm[kNR];                     // -m, the addend of the logits (0 before a segment's first tile)
+    float delta[kNR];                  // raise of the running max at the last update
+    float alpha[kNR];                  // 2^-delta
+    float red[kGroups][4][kGRows];     // per (group, lane quadrant, row): partial maxima or row sums
+    float qred[kGroups][4];            // per (group, quadrant): query magnitude maxima
+    float qc[2][kGroups];              // per query buffer and row group: logit scale / query scale
     int abort;
     int pad;
-    uint64_t kfull[2], kfree[2], vfull[2], pfull[2], pvfree[2], sfull[2], sfree[2], qready, done;
-    uint64_t rfull[kNS], rempty[kNS];
+    uint64_t sfull, sfree, kfull[2], pvfull, mma2done, qready[2], done;
+    uint64_t rfull[kStages], rempty[kStages];
     uint32_t tslot;
 };
-static_assert(sizeof(Misc) <= 3072, "misc block");
-
-__device__ __forceinline__ int64_t cta_of_tile(int64_t g, int64_t tt, int nc) { return ((g + 1) * nc - 1) / tt; }
+static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -163,6 +183,11 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
     return u2f(d);
 }
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // OR of `pred` over the `n` threads of named barrier `id`, which all wait here.
 __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool pred) {
@@ -177,20 +202,14 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool pred) {
 }
 
 // 16-byte shared store as inline asm: it stays ahead of the proxy fence and the mbarrier arrive
-// that publish it to the tensor cores (a plain store through a restrict pointer could be moved
-// past them).
+// that publish it to the tensor cores.
 __device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-
-// 16-byte global -> shared copy, zero-filled when src_bytes == 0
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ uint32_t ld_shared32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
 // int8 x4 -> two fp16x2 words, exactly: fp16(0x6400 | (x ^ 0x80)) = 1024 + x + 128.
@@ -207,263 +226,288 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-template <int K>
-__device__ __forceinline__ uint32_t code_pair(const uint32_t (&w)[12]) {
-    // 6-bit field (two consecutive 3-bit codes) at bit 6K of the 384-bit row
-    constexpr int bit = 6 * K, word = bit >> 5, off = bit & 31;
-    if constexpr (off <= 26) {
-        return (w[word] >> off) & 63u;
-    } else {
-        return ((w[word] >> off) | (w[word + 1] << (32 - off))) & 63u;
+// One token's q8_0 block (32 int8 codes) -> 16 fp16 pairs in this thread's TMEM lane at `taddr`.
+__device__ __forceinline__ void store_key_block(const uint4 (&kc)[2], uint32_t taddr) {
+    uint32_t r[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w[4] = {kc[h].x, kc[h].y, kc[h].z, kc[h].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) i8x4_to_f16x4(w[e], r[8 * h + 2 * e], r[8 * h + 2 * e + 1]);
     }
+    tc::tmem_st16(taddr, r);
 }
 
-// Four 16-byte chunks (dims 8C..8C+31) of one token's value row: centroid pairs looked up
-// (all sixteen issued before the stores) and scaled by the token's ||v|| * w.
+// Byte offset (times 128) of centroid-pair table entry for tokens (2C, 2C+1): their two 3-bit codes
+// are bits 6C .. 6C+5 of the 96-bit string (w2:w1:w0); returns idx << 7 (an entry is 32 lane copies
+// of 4 bytes).
 template <int C>
-__device__ __forceinline__ void store_v_quad(const uint32_t (&w)[12], const uint32_t* lut, uint32_t vstage,
-                                             uint32_t tok, __half2 nw2) {
-    uint32_t o[16];
-#define PKV_LUT(I) o[I] = lut[code_pair<4 * C + I>(w) * 32];
-    PKV_LUT(0) PKV_LUT(1) PKV_LUT(2) PKV_LUT(3) PKV_LUT(4) PKV_LUT(5) PKV_LUT(6) PKV_LUT(7)
-    PKV_LUT(8) PKV_LUT(9) PKV_LUT(10) PKV_LUT(11) PKV_LUT(12) PKV_LUT(13) PKV_LUT(14) PKV_LUT(15)
-#undef PKV_LUT
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&o[i]), nw2);
-        o[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        st_shared16(vstage + ((C + q) / 8) * 16384 + tc::sw128(tok, ((C + q) % 8) * 16), o[4 * q], o[4 * q + 1],
-                    o[4 * q + 2], o[4 * q + 3]);
-}
-
-// Row maxima (in M.red, relative to the running max for a rescale, absolute on a segment's
-// first tile) -> new running max and alpha per row of this group. With `scale_o`, O and
-// the per-slot row sums are scaled by alpha once MMA2 of the previous tile is done.
-__device__ __noinline__ void softmax_new_max(Misc& M, int grp, int tt, int rbase, int R, uint32_t gbar,
-                                             bool seg_first, int64_t j, uint32_t lane_addr, volatile int* abortp) {
-    tc::named_bar(gbar, 128);
-    if (tt < kGRows) {
-        const int r = rbase + tt;
-        const float mt = fmaxf(fmaxf(M.red[grp][0][tt], M.red[grp][1][tt]),
-                               fmaxf(M.red[grp][2][tt], M.red[grp][3][tt]));
-        if (seg_first) {
-            const float mn = r < R ? mt : INFINITY;
-            M.m[r] = mn;
-            M.nm[r] = -mn;
-            M.alpha[r] = 1.0f;
-        } else if (r < R && mt > 0.0f) {
-            const float mn = M.m[r] + mt;
-            M.alpha[r] = ex2(M.m[r] - mn);
-            M.m[r] = mn;
-            M.nm[r] = -mn;
-        } else {
-            M.alpha[r] = 1.0f;
-        }
-    }
-    tc::named_bar(gbar, 128);
-    if (!seg_first) {
-        // O must be scaled before MMA2 of this tile adds to it
-        tc::mbar_wait(tc::smem_u32(&M.pvfree[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1), abortp, kTimeoutNs);
-        tc::fence_after();
-#pragma unroll
-        for (int cc = 0; cc < kGRows / 16; ++cc) {
-            uint32_t to[16], tl[16];
-            tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
-            tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
-            tc::wait_ld();
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float a = M.alpha[rbase + 16 * cc + k];
-                to[k] = __float_as_uint(__uint_as_float(to[k]) * a);
-                tl[k] = __float_as_uint(__uint_as_float(tl[k]) * a);
-            }
-            tc::tmem_st16(lane_addr + kColO + rbase + 16u * cc, to);
-            tc::tmem_st16(lane_addr + kColL + rbase + 16u * cc, tl);
-        }
-        tc::wait_st();
+__device__ __forceinline__ uint32_t pair_off(uint32_t w0, uint32_t w1, uint32_t w2) {
+    constexpr int bit = 6 * C, word = bit >> 5, off = bit & 31;
+    const uint32_t lo = word == 0 ? w0 : (word == 1 ? w1 : w2);
+    if constexpr (off > 26) {   // the pair straddles two words
+        const uint32_t hi = word == 0 ? w1 : w2;
+        return __funnelshift_r(lo, hi, off - 7) & 0x1F80u;
+    } else if constexpr (off >= 7) {
+        return (lo >> (off - 7)) & 0x1F80u;
+    } else {
+        return (lo << (7 - off)) & 0x1F80u;
     }
 }
 
-// per-segment value scale w = 2^(8 - e), nmax = f * 2^e with f in [0.5, 1): ||v|| * w < 2^8
+// The 32 value codes of one coordinate (one 12-byte string) -> 16 fp16 centroid pairs.
+__device__ __forceinline__ void value_pairs(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t lut_lane,
+                                            uint32_t (&o)[16]) {
+#define PKV_PAIR(C) o[C] = ld_shared32(lut_lane | pair_off<C>(w0, w1, w2));
+    PKV_PAIR(0) PKV_PAIR(1) PKV_PAIR(2) PKV_PAIR(3) PKV_PAIR(4) PKV_PAIR(5) PKV_PAIR(6) PKV_PAIR(7)
+    PKV_PAIR(8) PKV_PAIR(9) PKV_PAIR(10) PKV_PAIR(11) PKV_PAIR(12) PKV_PAIR(13) PKV_PAIR(14) PKV_PAIR(15)
+#undef PKV_PAIR
+}
+
+// MMA1 of one tile, issued by one elected lane of the converged MMA warp: for each q8_0 block b,
+// S_b (TMEM columns tS + 64b) = key codes (TMEM columns aK + 16b + 8h, h = 0, 1) . queries (the
+// K-major descriptor bq advanced to dims 32b + 16h), then a commit to `bar`. All operand addresses
+// are formed inside one asm statement from three values, so issuing costs a few instructions.
+__device__ __forceinline__ void issue_mma1(uint32_t tS, uint32_t aK, uint64_t bq, uint32_t idesc, uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred P, T, F;\n .reg .b32 d1, d2, d3, a1, a2, a3, a4, a5, a6, a7;\n"
+        " .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n"
+        " elect.sync _|P, 0xffffffff;\n setp.ne.u32 T, 1, 0;\n setp.ne.u32 F, 0, 0;\n"
+        " add.u32 d1, %0, 64;\n add.u32 d2, %0, 128;\n add.u32 d3, %0, 192;\n"
+        " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n add.u32 a4, %1, 32;\n"
+        " add.u32 a5, %1, 40;\n add.u32 a6, %1, 48;\n add.u32 a7, %1, 56;\n"
+        " add.u64 b1, %2, 2;\n add.u64 b2, %2, 4;\n add.u64 b3, %2, 6;\n add.u64 b4, %2, 512;\n"
+        " add.u64 b5, %2, 514;\n add.u64 b6, %2, 516;\n add.u64 b7, %2, 518;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, F;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [d1], [a2], b2, %3, F;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [d2], [a4], b4, %3, F;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [d3], [a6], b6, %3, F;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [d1], [a3], b3, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [d2], [a5], b5, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [d3], [a7], b7, %3, T;\n"
+        " @P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n}" ::"r"(tS),
+        "r"(aK), "l"(bq), "r"(idesc), "r"(bar)
+        : "memory");
+}
+
+// MMA2 of one tile: O (TMEM tO) += value centroids (TMEM columns tV + 8ks) . P' (MN-major descriptor
+// bp advanced by 16 tokens = 2 KB per step), ks = 0..7; `fresh` starts the accumulator (a segment's
+// first tile); then a commit to `bar`.
+__device__ __forceinline__ void issue_mma2(uint32_t tO, uint32_t tV, uint64_t bp, uint32_t idesc, uint32_t fresh,
+                                           uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred P, T, A0;\n .reg .b32 a1, a2, a3, a4, a5, a6, a7;\n"
+        " .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n"
+        " elect.sync _|P, 0xffffffff;\n setp.ne.u32 T, 1, 0;\n setp.eq.u32 A0, %4, 0;\n"
+        " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n add.u32 a4, %1, 32;\n"
+        " add.u32 a5, %1, 40;\n add.u32 a6, %1, 48;\n add.u32 a7, %1, 56;\n"
+        " add.u64 b1, %2, 128;\n add.u64 b2, %2, 256;\n add.u64 b3, %2, 384;\n add.u64 b4, %2, 512;\n"
+        " add.u64 b5, %2, 640;\n add.u64 b6, %2, 768;\n add.u64 b7, %2, 896;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, A0;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, T;\n"
+        " @P tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, T;\n"
+        " @P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n}" ::"r"(tO),
+        "r"(tV), "l"(bp), "r"(idesc), "r"(fresh), "r"(bar)
+        : "memory");
+}
+
+// One elected lane commits all of this warp's earlier MMAs to `bar`.
+__device__ __forceinline__ void commit_elected(uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n"
+        " @P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+        : "memory");
+}
+
+// per-unit value scale w = 2^(7 - e), nmax = f * 2^e with f in [0.5, 1): ||v|| * w <= 2^7
 __device__ __forceinline__ float unit_wscale(float nmax) {
     int en = 0;
     if (nmax > 0.0f) frexpf(nmax, &en);
-    return nmax > 0.0f ? ldexpf(1.0f, 8 - en) : 1.0f;
+    return nmax > 0.0f ? ldexpf(1.0f, 7 - en) : 1.0f;
 }
 
-// Segment prologue (all row groups, every softmax thread): the unit's queries in fp16 scaled by a power
-// of two into the MMA1 operand, the logit scale and the value scale w.
-template <bool QBF16>
-__device__ __noinline__ void softmax_prologue(const uint16_t* __restrict__ q, const float* __restrict__ nmax, int64_t u,
-                                              int r0, int H, int A, int Hq, int G, int R, float scale_log2,
-                                              uint8_t* sQ, Misc& M, int si, int wi, int lane) {
-    const int layer = (int)(u / H), kvh = (int)(u % H);
-    uint4 qv[1024 / kSmThreads];
-    float qm = 0.0f;
-#pragma unroll
-    for (int m = 0; m < 1024 / kSmThreads; ++m) {
-        const int cid = si + kSmThreads * m;
-        qv[m] = make_uint4(0u, 0u, 0u, 0u);
-        if (cid < R * 16) {
-            const int r = cid >> 4, dc = cid & 15;
-            const int a = (r0 + r) / G, gq = (r0 + r) % G;
-            qv[m] = __ldg(reinterpret_cast<const uint4*>(
-                              q + (((int64_t)layer * A + a) * Hq + kvh * G + gq) * kD) + dc);
-            const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float lo, hi;
-                if (QBF16) {
-                    lo = __uint_as_float(wv[e] << 16);
-                    hi = __uint_as_float(wv[e] & 0xFFFF0000u);
-                } else {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-                    lo = f.x;
-                    hi = f.y;
-                }
-                qm = fmaxf(qm, fmaxf(fabsf(lo), fabsf(hi)));
+// Position in this CTA's contiguous (segment, tile) list, advanced one tile at a time.
+struct Cursor {
+    int64_t seg, unit;
+    int ti, rg;
+    __device__ __forceinline__ void adv(int nt, int nrg) {
+        if (++ti == nt) {
+            ti = 0;
+            ++seg;
+            if (++rg == nrg) {
+                rg = 0;
+                ++unit;
             }
         }
     }
+};
+
+// Query rows of one segment handled by this worker thread: row 16g + 4qd + lane/8 of the segment,
+// dims 16c .. 16c+15 with c = lane % 8 (two 16-byte loads; zero for padding rows).
+__device__ __forceinline__ void q_load(const TcParams& P, const Cursor& c, int g, int qd, int lane, uint4 (&raw)[2]) {
+    const int r = kGRows * g + 4 * qd + (lane >> 3), ch = lane & 7;
+    const int R0 = c.rg * kNR + r;
+    raw[0] = raw[1] = make_uint4(0u, 0u, 0u, 0u);
+    if (R0 < P.Rtot) {
+        const int layer = (int)(c.unit / P.p.H), kvh = (int)(c.unit % P.p.H);
+        const int a = R0 / P.G, gq = R0 % P.G;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            P.q + (((int64_t)layer * P.A + a) * P.Hq + kvh * P.G + gq) * kD + 16 * ch);
+        raw[0] = __ldg(src);
+        raw[1] = __ldg(src + 1);
+    }
+}
+
+// The segment's queries for this row group in fp16, scaled by fq = 2^(15 - e) where the group's
+// largest magnitude is f * 2^e (f in [0.5, 1)), into query buffer `qbuf` (the B operand of MMA1,
+// K-major, 128-byte swizzle: two chunks of 64 dims x [64 rows][128 B]); the group's combine
+// constant (logit scale in log2 units / fq) goes to M.qc. Ends with the buffer published to the
+// MMA issuer (one arrival per warp) and a group barrier.
+template <bool QBF16>
+__device__ __forceinline__ void q_store(const uint4 (&raw)[2], uint32_t qbuf_u, Misc& M, int buf, int g, int qd,
+                                        int lane, float scale_log2) {
+    float x[16];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
-    if (lane == 0) M.qred[wi] = qm;
-    tc::named_bar(kBarSoftmax, kSmThreads);
-    float qmax = 0.0f;
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w[4] = {raw[h].x, raw[h].y, raw[h].z, raw[h].w};
 #pragma unroll
-    for (int w8 = 0; w8 < kSmWarps; ++w8) qmax = fmaxf(qmax, M.qred[w8]);
+        for (int e = 0; e < 4; ++e) {
+            if (QBF16) {
+                x[8 * h + 2 * e] = __uint_as_float(w[e] << 16);
+                x[8 * h + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            } else {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                x[8 * h + 2 * e] = f.x;
+                x[8 * h + 2 * e + 1] = f.y;
+            }
+        }
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(x[i]));
+    const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));   // magnitudes order as uints
+    if (lane == 0) M.qred[g][qd] = __uint_as_float(mb);
+    tc::named_bar(kBarGroup + g, 128);
+    const float qmax = fmaxf(fmaxf(M.qred[g][0], M.qred[g][1]), fmaxf(M.qred[g][2], M.qred[g][3]));
     int eq = 0;
     if (qmax > 0.0f) frexpf(qmax, &eq);
-    const float fq = qmax > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;  // qmax * fq in [2^14, 2^15)
+    const float fq = qmax > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;   // qmax * fq in [2^14, 2^15)
+    uint32_t hv[8];
 #pragma unroll
-    for (int m = 0; m < 1024 / kSmThreads; ++m) {
-        const int cid = si + kSmThreads * m;
-        if (cid < kNR * 16) {
-            const int r = cid >> 4, dc = cid & 15;
-            const uint32_t wv[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
-            uint32_t hv[4];
+    for (int i = 0; i < 8; ++i) {
+        const __half2 h2 = __floats2half2_rn(x[2 * i] * fq, x[2 * i + 1] * fq);
+        hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    const int r = kGRows * g + 4 * qd + (lane >> 3), ch = lane & 7;
+    const uint32_t rowb = qbuf_u + (uint32_t)(ch >> 2) * 8192u + (uint32_t)r * 128u;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float lo = 0.0f, hi = 0.0f;
-                if (r < R) {
-                    if (QBF16) {
-                        lo = __uint_as_float(wv[e] << 16);
-                        hi = __uint_as_float(wv[e] & 0xFFFF0000u);
-                    } else {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-                        lo = f.x;
-                        hi = f.y;
-                    }
-                }
-                const __half2 h = __floats2half2_rn(lo * fq, hi * fq);
-                hv[e] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            st_shared16(tc::smem_u32(sQ) + (dc >> 3) * 8192 + tc::sw128(r, (dc & 7) * 16), hv[0], hv[1], hv[2], hv[3]);
-        }
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t chunk = (uint32_t)(((ch & 3) * 2 + h) ^ (r & 7));
+        st_shared16(rowb + (chunk << 4), hv[4 * h], hv[4 * h + 1], hv[4 * h + 2], hv[4 * h + 3]);
     }
-    if (si == 0) {
-        M.scale_eff = scale_log2 * 16.0f / fq;  // keys are stored in TMEM as s * code * 2^-4
-        M.wscale = unit_wscale(nmax[u]);
-    }
+    if (qd == 0 && lane == 0) M.qc[buf][g] = scale_log2 / fq;
     tc::fence_proxy_async();
-    tc::named_bar(kBarSoftmax, kSmThreads);
-    if (si == 0) tc::mbar_arrive(tc::smem_u32(&M.qready));
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.qready[buf]));
+    tc::named_bar(kBarGroup + g, 128);
 }
 
-// Segment epilogue (one row group): row sums over the token slots, then the rows' O^T columns
-// (divided by w) and (m, l) written as the partial for (unit, piece) `slot`.
-__device__ __noinline__ void softmax_epilogue(Misc& M, int s, uint32_t ph, volatile int* abortp, uint32_t lane_addr,
-                                              int grp, int wq, int lane, int tt, int rbase, int R, int RS,
-                                              uint32_t gbar, int64_t slot, float* __restrict__ ws_acc,
-                                              float* __restrict__ ws_ml) {
-    tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph, abortp, kTimeoutNs);
-    tc::fence_after();
-    tc::wait_st();
+// Row sums of this row group over the 128 token slots (lanes x quadrants) at the end of a segment
+// piece, written with the rows' running maxima as the piece's (m, l) partial.
+__device__ __forceinline__ void write_row_stats(const float2 (&l)[8], Misc& M, int g, int qd, int lane, int R,
+                                                float* __restrict__ ml_slot) {
+    float v[16];
 #pragma unroll
-    for (int cc = 0; cc < kGRows / 16; ++cc) {
-        uint32_t tl[16];
-        tc::tmem_ld16(lane_addr + kColL + rbase + 16u * cc, tl);
-        tc::wait_ld();
+    for (int k = 0; k < 8; ++k) {
+        v[2 * k] = l[k].x;
+        v[2 * k + 1] = l[k].y;
+    }
+    // transposing butterfly: each round halves the rows a lane keeps and sums them over lane pairs
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            float v = __uint_as_float(tl[k]);
+    for (int k = 0; k < 8; ++k) {
+        const bool up = (lane & 16) != 0;
+        const float send = up ? v[k] : v[k + 8], keep = up ? v[k + 8] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 16 * cc + k) M.red[grp][wq][16 * cc + k] = v;
+    for (int k = 0; k < 4; ++k) {
+        const bool up = (lane & 8) != 0;
+        const float send = up ? v[k] : v[k + 4], keep = up ? v[k + 4] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const bool up = (lane & 4) != 0;
+        const float send = up ? v[k] : v[k + 2], keep = up ? v[k + 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+        const bool up = (lane & 2) != 0;
+        const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    const int row = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+    if ((lane & 1) == 0) M.red[g][qd][row] = v[0];
+    tc::named_bar(kBarGroup + g, 128);
+    if (qd == 0 && lane < kGRows) {
+        const int r = kGRows * g + lane;
+        if (r < R) {
+            ml_slot[2 * r] = M.m[r];
+            ml_slot[2 * r + 1] = (M.red[g][0][lane] + M.red[g][1][lane]) + (M.red[g][2][lane] + M.red[g][3][lane]);
         }
     }
-    tc::named_bar(gbar, 128);
-    const float unscale = 1.0f / M.wscale;
-#pragma unroll
-    for (int cc = 0; cc < kGRows / 16; ++cc) {
-        uint32_t to[16];
-        tc::tmem_ld16(lane_addr + kColO + rbase + 16u * cc, to);
-        tc::wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int r = rbase + 16 * cc + k;
-            if (r < R) ws_acc[(slot * RS + r) * kD + tt] = __uint_as_float(to[k]) * unscale;
-        }
-    }
-    if (tt < kGRows && rbase + tt < R) {
-        const int r = rbase + tt;
-        ws_ml[(slot * RS + r) * 2] = M.m[r];
-        ws_ml[(slot * RS + r) * 2 + 1] =
-            M.red[grp][0][tt] + M.red[grp][1][tt] + M.red[grp][2][tt] + M.red[grp][3][tt];
-    }
-    tc::fence_before();
-    tc::named_bar(kBarSoftmax, kSmThreads);
 }
 
 template <bool QBF16>
-__global__ void __launch_bounds__(kThreadsTc, 1)
-    attend_tc_kernel(const TcParams P) {
+__global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u = tc::smem_u32(smem_raw);
-    uint8_t* sm = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
-    uint8_t* sQ = sm + kSmQ;
-    uint8_t* sV = sm + kSmV;
-    uint8_t* sP = sm + kSmP;
-    uint8_t* sR = sm + kSmRaw;
-    uint8_t* sK = sm + kSmK;
+    uint8_t* sm = smem_raw + (((raw_u + 8191u) & ~8191u) - raw_u);
+    const uint32_t sm_u = tc::smem_u32(sm);
     uint32_t* lut = reinterpret_cast<uint32_t*>(sm + kSmLut);
     Misc& M = *reinterpret_cast<Misc*>(sm + kSmMisc);
     volatile int* abortp = &M.abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t TT = P.total_tiles;
-    const int c = blockIdx.x;
-    const int64_t g0 = (int64_t)c * TT / P.nctas;
-    const int64_t g1 = (int64_t)(c + 1) * TT / P.nctas;
+    const int cta = blockIdx.x;
+    const int64_t g0 = (int64_t)cta * TT / P.nctas;
+    const int64_t g1 = (int64_t)(cta + 1) * TT / P.nctas;
     const int n = (int)(g1 - g0);
-    const int nt = P.nt;
-    const int64_t cap = P.p.cap;
+    const int nt = P.nt, nrg = P.nrg;
+    Cursor c0;
+    c0.seg = g0 / nt;
+    c0.ti = (int)(g0 - c0.seg * nt);
+    c0.unit = c0.seg / nrg;
+    c0.rg = (int)(c0.seg - c0.unit * nrg);
 
-    // ---- set-up: barriers, codebook pairs, TMEM
+    // ---- set-up: barriers, centroid-pair table, TMEM
     if (tid == 0) {
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(tc::smem_u32(&M.kfull[s]), 128);
-            tc::mbar_init(tc::smem_u32(&M.kfree[s]), 1);
-            tc::mbar_init(tc::smem_u32(&M.vfull[s]), 128);
-            tc::mbar_init(tc::smem_u32(&M.pfull[s]), kSmThreads);
-            tc::mbar_init(tc::smem_u32(&M.pvfree[s]), 1);
-            tc::mbar_init(tc::smem_u32(&M.sfull[s]), 1);
-            tc::mbar_init(tc::smem_u32(&M.sfree[s]), kSmThreads);
-        }
-        for (int s = 0; s < kNS; ++s) {
-            tc::mbar_init(tc::smem_u32(&M.rfull[s]), 1);
-            tc::mbar_init(tc::smem_u32(&M.rempty[s]), 128);
-        }
-        tc::mbar_init(tc::smem_u32(&M.qready), 1);
+        tc::mbar_init(tc::smem_u32(&M.sfull), 1);
+        tc::mbar_init(tc::smem_u32(&M.sfree), kWorkers);
+        tc::mbar_init(tc::smem_u32(&M.kfull[0]), kWorkers);
+        tc::mbar_init(tc::smem_u32(&M.kfull[1]), kWorkers);
+        tc::mbar_init(tc::smem_u32(&M.pvfull), kWorkers);
+        tc::mbar_init(tc::smem_u32(&M.mma2done), 1);
+        tc::mbar_init(tc::smem_u32(&M.qready[0]), kWorkers);
+        tc::mbar_init(tc::smem_u32(&M.qready[1]), kWorkers);
         tc::mbar_init(tc::smem_u32(&M.done), 1);
+        for (int st = 0; st < kStages; ++st) {
+            tc::mbar_init(tc::smem_u32(&M.rfull[st]), 1);
+            tc::mbar_init(tc::smem_u32(&M.rempty[st]), kWorkers);
+        }
         M.abort = 0;
         tc::mbar_init_fence();
     }
     for (int e = tid; e < 64 * 32; e += kThreadsTc) {
-        const int idx = e >> 5;
+        const int idx = e >> 5;   // two 3-bit codes: the even token in bits 0..2, the odd one in 3..5
         const __half lo = __float2half_rn(centroid_of(idx & 7));
         const __half hi = __float2half_rn(centroid_of(idx >> 3));
         lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
@@ -474,374 +518,373 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc::fence_after();
     const uint32_t tbase = M.tslot;
 
-    if (warp == kWarpTma) {
-        // =============================== TMA: scales / value codes / norms into the ring
-        if (lane == 0) {
-            int issued = 0;
-            int64_t sg = g0 / nt;                  // segment
-            int64_t u = sg / P.nrg;                // its pool unit
-            int ti = (int)(g0 - sg * nt);
-            for (int j = 0; j < n && !*abortp; ++j) {
-                const int st = j & (kNS - 1);
-                if (j >= kNS &&
-                    !tc::mbar_wait(tc::smem_u32(&M.rempty[st]), (uint32_t)(((j / kNS) - 1) & 1), abortp, kTimeoutNs))
-                    break;
-                const int64_t row0 = u * cap + (int64_t)ti * kTile;
-                if (++ti == nt) {
-                    ti = 0;
-                    u = ++sg / P.nrg;
-                }
-                const uint32_t dst = tc::smem_u32(sR + st * kRawStage);
-                const uint32_t bar = tc::smem_u32(&M.rfull[st]);
-                tc::mbar_arrive_expect_tx(bar, kRawBytes);
-                tc::bulk_g2s(dst + kRawS, P.p.ks + row0 * (kD / kQ8Block), 1024, bar);
-                tc::bulk_g2s(dst + kRawV, P.p.vc + row0 * (3 * kD / 8), 6144, bar);
-                tc::bulk_g2s(dst + kRawN, P.p.vn + row0, 256, bar);
-                issued = j + 1;
+    if (warp < kWorkers) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegWorker));
+        // =============================== workers
+        const int g = warp >> 2;                   // row group, key block, token quarter
+        const int qd = warp & 3;                   // TMEM lane quadrant
+        const int t = qd * 32 + lane;              // TMEM lane: token (keys, softmax) and coordinate (values)
+        const uint32_t lane_addr = tbase + ((uint32_t)(qd * 32) << 16);
+        const uint32_t lut_lane = sm_u + kSmLut + (uint32_t)lane * 4u;
+        const uint32_t rbar = kBarRed + g;
+        const int64_t seg0 = c0.seg;
+        // this thread's offsets inside a ring stage
+        const uint32_t key_off = kStKeys + (uint32_t)t * 128u;                  // + swizzled chunk
+        const uint32_t key_sw = (uint32_t)(t & 7);
+        const uint32_t val_off = kStVals + (uint32_t)(g * kD + t) * 12u;
+        const uint32_t sc_off = kStScales + (uint32_t)t * 8u;
+        const uint32_t nv_off = kStNorms + (uint32_t)t * 2u;
+        // key operand of tile j (ring stage j % kStages, already full) into TMEM key buffer j & 1
+        auto put_keys = [&](int j) {
+            const uint32_t st = sm_u + kSmRing + (uint32_t)(j % kStages) * kStageBytes + key_off;
+            uint4 kc[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t a = st + ((((uint32_t)(2 * g + h)) ^ key_sw) << 4);
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(kc[h].x), "=r"(kc[h].y), "=r"(kc[h].z), "=r"(kc[h].w)
+                             : "r"(a));
             }
-            // drain: never leave copies in flight into shared memory that is about to be released
-            for (int j = issued > kNS ? issued - kNS : 0; j < issued; ++j) {
-                volatile int dummy = 0;
-                tc::mbar_wait(tc::smem_u32(&M.rfull[j & (kNS - 1)]), (uint32_t)((j / kNS) & 1), &dummy, 50000000ull);
+            store_key_block(kc, lane_addr + kColK + (uint32_t)(j & 1) * 64u + 16u * g);
+            tc::wait_st();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.kfull[j & 1]));
+        };
+        auto wait_stage = [&](int j) {
+            tc::mbar_wait(tc::smem_u32(&M.rfull[j % kStages]), (uint32_t)((j / kStages) & 1), abortp, kTimeoutNs);
+        };
+
+        // prologue: tile 0's key operand and the first segments' queries
+        Cursor c1 = c0, c2 = c0;
+        c1.adv(nt, nrg);
+        c2 = c1;
+        c2.adv(nt, nrg);
+        {
+            uint4 qr[2];
+            q_load(P, c0, g, qd, lane, qr);
+            q_store<QBF16>(qr, sm_u + kSmQ, M, 0, g, qd, lane, P.scale_log2);
+            if (n > 1 && c1.ti == 0) {
+                q_load(P, c1, g, qd, lane, qr);
+                q_store<QBF16>(qr, sm_u + kSmQ + 16384u, M, 1, g, qd, lane, P.scale_log2);
             }
+            wait_stage(0);
+            put_keys(0);
         }
-    } else if (warp < 8) {
-        // =============================== producers: two groups of four warps take alternate tiles
-        // (group pg: tiles pg, pg + 2, ...; TMEM/shared stage pg). Each thread owns one token slot
-        // (= TMEM lane) and writes that token's exact key halves to TMEM, then its norm-scaled value
-        // centroids to shared memory.
-        const int pg = warp >> 2;
-        const uint32_t q4 = (uint32_t)(warp & 3);
-        const uint32_t lane_addr = tbase + ((q4 * 32u) << 16);
-        const uint32_t t = q4 * 32u + (uint32_t)lane;
-        const uint32_t krow = tc::smem_u32(sK) + t * kKRow + (uint32_t)(2 * pg) * kKStage;
-        auto adv2 = [&](int64_t& sg, int& tix) {   // two tiles on, across segments
-            tix += 2;
-            while (tix >= nt) {
-                tix -= nt;
-                ++sg;
-            }
-        };
-        int64_t u_n = (g0 + pg) / nt;              // segment of the next key-row copy
-        int ti_n = (int)((g0 + pg) - u_n * nt);
-        int64_t pu_n = u_n / P.nrg;                // its pool unit and row group, advanced incrementally
-        int rg_n = (int)(u_n - pu_n * P.nrg);
-        int kk = 0;
-        // copy the key row of this token slot for this group's tile jj into the group's stage kk & 1
-        auto issue_k = [&](int jj) {
-            if (jj < n) {
-                const int64_t tok = (int64_t)ti_n * kTile + t;
-                const bool ok = tok < P.n_ctx;
-                const int8_t* src = P.p.kq + (pu_n * cap + (ok ? tok : 0)) * kD;
-                const uint32_t dst = krow + (uint32_t)(kk & 1) * kKStage;
+
+        Cursor cur = c0;
+        float2 l[8];
+        float cst = 0.0f, wsc = 1.0f;
+        int R = 0;
+        // a finished segment piece whose O is read out at the next tile (after its last MMA2)
+        bool epi = false;
+        int epi_R = 0;
+        float epi_inv_w = 1.0f;
+        int64_t epi_slot = 0;
+        for (int i = 0; i < n; ++i) {
+            const bool first = (i == 0) || (cur.ti == 0);
+            const bool last = (i == n - 1) || (cur.ti == nt - 1);
+            if (first) {
+                R = min(kNR, P.Rtot - kNR * cur.rg);
+                cst = M.qc[(cur.seg - seg0) & 1][g];
+                wsc = unit_wscale(P.p.nmax[cur.unit]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) cp_async16(dst + 16u * i, src + 16 * i, ok ? 16u : 0u);
-                ti_n += 2;
-                while (ti_n >= nt) {
-                    ti_n -= nt;
-                    if (++rg_n == P.nrg) {
-                        rg_n = 0;
-                        ++pu_n;
-                    }
+                for (int k = 0; k < 8; ++k) l[k] = make_float2(0.0f, 0.0f);
+            }
+            const uint32_t stg = sm_u + kSmRing + (uint32_t)(i % kStages) * kStageBytes;
+            // -- a. key operand of tile i+1 (its buffer was last read by MMA1(i-1), complete), so that
+            //       MMA1(i+1) can start as soon as S(i) has been read; queries of tile i+2's segment
+            if (i + 1 < n) {
+                wait_stage(i + 1);
+                put_keys(i + 1);
+            }
+            const bool qprep = (i + 2 < n) && c2.ti == 0;
+            uint4 qr[2] = {};
+            if (qprep) q_load(P, c2, g, qd, lane, qr);
+
+            // -- b. S(i) = MMA1(i)
+            tc::mbar_wait(tc::smem_u32(&M.sfull), (uint32_t)(i & 1), abortp, kTimeoutNs);
+            tc::fence_after();
+
+            // -- c. logits d = sum_b c_b S_b - m (absolute on a segment's first tile)
+            uint2 scw;
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(scw.x), "=r"(scw.y) : "r"(stg + sc_off));
+            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&scw.x));
+            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&scw.y));
+            const float cb0 = s01.x * cst, cb1 = s01.y * cst, cb2 = s23.x * cst, cb3 = s23.y * cst;
+            float2 d[8];
+            {
+                // -m per row (the first tile of a segment takes absolute logits)
+                const float4* nmv = reinterpret_cast<const float4*>(&M.nm[kGRows * g]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 v = first ? make_float4(0.f, 0.f, 0.f, 0.f) : nmv[k];
+                    d[2 * k] = make_float2(v.x, v.y);
+                    d[2 * k + 1] = make_float2(v.z, v.w);
+                }
+                uint32_t sa[16], sb[16];
+                tc::tmem_ld16(lane_addr + kColS + 16u * g, sa);
+                tc::tmem_ld16(lane_addr + kColS + 64u + 16u * g, sb);
+                tc::wait_ld();
+                const float2 c0x = make_float2(cb0, cb0), c1x = make_float2(cb1, cb1);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    d[k] = fma2(c0x, make_float2(__uint_as_float(sa[2 * k]), __uint_as_float(sa[2 * k + 1])), d[k]);
+                    d[k] = fma2(c1x, make_float2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1])), d[k]);
+                }
+                tc::tmem_ld16(lane_addr + kColS + 128u + 16u * g, sa);
+                tc::tmem_ld16(lane_addr + kColS + 192u + 16u * g, sb);
+                tc::wait_ld();
+                // S(i) has been read for the last time: MMA1(i+1) may overwrite it
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.sfree));
+                const float2 c2x = make_float2(cb2, cb2), c3x = make_float2(cb3, cb3);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    d[k] = fma2(c2x, make_float2(__uint_as_float(sa[2 * k]), __uint_as_float(sa[2 * k + 1])), d[k]);
+                    d[k] = fma2(c3x, make_float2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1])), d[k]);
                 }
             }
-            ++kk;
-            cp_async_commit();
-        };
-        issue_k(pg);
-        int64_t u = (g0 + pg) / nt;                // segment of the current tile
-        int ti = (int)((g0 + pg) - u * nt);
-        float wscale = pg < n ? unit_wscale(P.p.nmax[u / P.nrg]) : 1.0f;
-        const int s = pg;
-        int k = 0;
-        // The loop always runs to its end so that all 128 threads of the group meet at the same
-        // named barriers; after an abort every wait returns at once and the data are ignored.
-        for (int j = pg; j < n; j += 2, ++k) {
-            const uint32_t ph = (uint32_t)((j >> 1) & 1);
-            const int st = j & (kNS - 1);
-            const bool valid = (int64_t)ti * kTile + t < P.n_ctx;
-            issue_k(j + 2);
-            tc::mbar_wait(tc::smem_u32(&M.rfull[st]), (uint32_t)((j / kNS) & 1), abortp, kTimeoutNs);
-            const uint8_t* raw = sR + st * kRawStage;
-            const uint2 sraw = valid ? *reinterpret_cast<const uint2*>(raw + kRawS + t * 8) : make_uint2(0u, 0u);
-            uint32_t w[12];
+            const int64_t tok = (int64_t)cur.ti * kTile + t;
+            const bool valid = tok < P.n_ctx;
+            if ((int64_t)(cur.ti + 1) * kTile > P.n_ctx && !valid) {
 #pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                const uint4 x = *reinterpret_cast<const uint4*>(raw + kRawV + t * 48 + 16 * i);
-                w[4 * i] = x.x;
-                w[4 * i + 1] = x.y;
-                w[4 * i + 2] = x.z;
-                w[4 * i + 3] = x.w;
+                for (int k = 0; k < 8; ++k) d[k] = make_float2(-INFINITY, -INFINITY);
             }
-            const unsigned short nb = *reinterpret_cast<const unsigned short*>(raw + kRawN + t * 2);
-            // the ring stage is refilled by the TMA (async proxy): order these reads before that write
+            float dmax = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dmax = max3f(dmax, d[k].x, d[k].y);
+            // -- lazy rescale: only when some logit of the row group exceeds its running max by 2^tau
+            bool resc = false;
+            if (first || bar_any(rbar, 128, dmax > kTau)) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float v0 = tc::warp_max(d[k].x);
+                    const float v1 = tc::warp_max(d[k].y);
+                    if (lane == 2 * k) M.red[g][qd][2 * k] = v0;
+                    if (lane == 2 * k + 1) M.red[g][qd][2 * k + 1] = v1;
+                }
+                tc::named_bar(kBarGroup + g, 128);
+                if (qd == 0 && lane < kGRows) {
+                    const int r = kGRows * g + lane;
+                    const float mt = fmaxf(fmaxf(M.red[g][0][lane], M.red[g][1][lane]),
+                                           fmaxf(M.red[g][2][lane], M.red[g][3][lane]));
+                    float dl = 0.0f, al = 1.0f;
+                    if (first) {
+                        dl = r < R ? mt : INFINITY;   // padding rows: d = -inf from now on
+                        M.m[r] = dl;
+                        M.nm[r] = -dl;
+                    } else if (r < R && mt > 0.0f) {
+                        dl = mt;
+                        al = ex2(-mt);
+                        M.m[r] += mt;
+                        M.nm[r] = -M.m[r];
+                    }
+                    M.delta[r] = dl;
+                    M.alpha[r] = al;
+                }
+                tc::named_bar(kBarGroup + g, 128);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float2 dl = *reinterpret_cast<const float2*>(&M.delta[kGRows * g + 2 * k]);
+                    d[k] = make_float2(d[k].x - dl.x, d[k].y - dl.y);
+                    if (!first) l[k] = mul2(l[k], *reinterpret_cast<const float2*>(&M.alpha[kGRows * g + 2 * k]));
+                }
+                resc = !first;
+            }
+            // -- d. probabilities: p = 2^d summed into l; P' = p * ||v|| * w in fp16
+            uint32_t nvb;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(nvb) : "r"(stg + nv_off));
+            const float nwf = valid ? __half2float(__ushort_as_half((unsigned short)nvb)) * wsc : 0.0f;
+            const float2 nw2 = make_float2(nwf, nwf);
+            uint32_t pk[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 pr = make_float2(ex2(d[k].x), ex2(d[k].y));
+                l[k] = add2(l[k], pr);
+                const float2 pw = mul2(pr, nw2);
+                const __half2 h = __floats2half2_rn(pw.x, pw.y);
+                pk[k] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            // -- e. value operand of tile i: this coordinate's centroids for token quarter g
+            uint32_t vv[16];
+            {
+                uint32_t w0, w1, w2;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(stg + val_off));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(stg + val_off + 4u));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w2) : "r"(stg + val_off + 8u));
+                value_pairs(w0, w1, w2, lut_lane, vv);
+            }
+            // stage i has been read for the last time (its keys in the previous iteration): the TMA
+            // (an async-proxy write) may refill it
             tc::fence_proxy_async();
-            tc::mbar_arrive(tc::smem_u32(&M.rempty[st]));
-            cp_async_wait<1>();   // this tile's key row has landed (the next one may be in flight)
-            const uint8_t* kr_s = sK + (2 * pg + (k & 1)) * kKStage + t * kKRow;
-            // keys: k_hat = s_b * code (times 2^-4 against fp16 overflow) as an exact fp16 pair
-            // hi = fp16(k_hat), lo = fp16(k_hat - hi): the product has <= 18 significant bits, hi + lo
-            // holds 22, so hi + lo = k_hat and MMA1 over hi then lo gives the exact q . k_hat sums.
-            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.kfree[s]), ph ^ 1u, abortp, kTimeoutNs);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.rempty[i % kStages]));
+
+            // -- f. after MMA2(i-1): write out a finished piece's O, rescale O, publish V'(i), P'(i)
+            if (i > 0) {
+                tc::mbar_wait(tc::smem_u32(&M.mma2done), (uint32_t)((i - 1) & 1), abortp, kTimeoutNs);
+                tc::fence_after();
+            }
+            if (epi) {
+                uint32_t ov[16];
+                tc::tmem_ld16(lane_addr + kColO + 16u * g, ov);
+                tc::wait_ld();
+                float* acc = P.ws_acc + epi_slot * P.RS * kD;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {   // q8_0 block qq = dims 32qq .. 32qq+31
-                const uint32_t sw = (qq < 2 ? sraw.x : sraw.y) >> (16 * (qq & 1));
-                __half2 sc = __half2half2(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
-                sc = __hmul2(sc, __half2half2(__ushort_as_half((unsigned short)0x2C00)));  // * 2^-4
-                uint32_t rh[16], rl[16];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 kr = *reinterpret_cast<const uint4*>(kr_s + 32 * qq + 16 * h);
-                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t c01, c23;
-                        i8x4_to_f16x4(kw[e], c01, c23);
-                        const __half2 h01 = __hmul2(*reinterpret_cast<const __half2*>(&c01), sc);
-                        const __half2 h23 = __hmul2(*reinterpret_cast<const __half2*>(&c23), sc);
-                        const __half2 l01 = __hfma2(*reinterpret_cast<const __half2*>(&c01), sc, __hneg2(h01));
-                        const __half2 l23 = __hfma2(*reinterpret_cast<const __half2*>(&c23), sc, __hneg2(h23));
-                        rh[h * 8 + 2 * e] = *reinterpret_cast<const uint32_t*>(&h01);
-                        rh[h * 8 + 2 * e + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-                        rl[h * 8 + 2 * e] = *reinterpret_cast<const uint32_t*>(&l01);
-                        rl[h * 8 + 2 * e + 1] = *reinterpret_cast<const uint32_t*>(&l23);
-                    }
+                for (int k = 0; k < kGRows; ++k) {
+                    const int r = kGRows * g + k;
+                    if (r < epi_R) acc[r * kD + t] = __uint_as_float(ov[k]) * epi_inv_w;
                 }
-                tc::tmem_st16(lane_addr + kColK + 128u * s + 16u * qq, rh);
-                tc::tmem_st16(lane_addr + kColK + 128u * s + 64u + 16u * qq, rl);
+                epi = false;
+            }
+            if (resc) {
+                uint32_t ox[16];
+                tc::tmem_ld16(lane_addr + kColO + 16u * g, ox);
+                tc::wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    ox[k] = __float_as_uint(__uint_as_float(ox[k]) * M.alpha[kGRows * g + k]);
+                tc::tmem_st16(lane_addr + kColO + 16u * g, ox);
+            }
+            tc::tmem_st16(lane_addr + kColV + 16u * g, vv);
+            {
+                // P'^T rows (token t) of the MN-major B operand, 128-byte swizzle: this thread's 16 rows
+                // are the 16-byte chunks 2g and 2g+1 of the token's 128-byte row
+                const uint32_t prow = sm_u + kSmP + (uint32_t)(i & 1) * 16384u + (uint32_t)t * 128u;
+                st_shared16(prow + ((uint32_t)((2 * g) ^ (t & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+                st_shared16(prow + ((uint32_t)((2 * g + 1) ^ (t & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
             }
             tc::wait_st();
             tc::fence_before();
-            tc::mbar_arrive(tc::smem_u32(&M.kfull[s]));
-            // values: packed 3-bit codes -> centroids * ||v|| * w in fp16, token-major rows
-            const float nw = valid ? __half2float(__ushort_as_half(nb)) * wscale : 0.0f;
-            const __half2 nw2 = __float2half2_rn(nw);
-            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
-            const uint32_t vst = tc::smem_u32(sV) + s * 32768;
-            store_v_quad<0>(w, lut + lane, vst, t, nw2);
-            store_v_quad<4>(w, lut + lane, vst, t, nw2);
-            store_v_quad<8>(w, lut + lane, vst, t, nw2);
-            store_v_quad<12>(w, lut + lane, vst, t, nw2);
             tc::fence_proxy_async();
-            tc::mbar_arrive(tc::smem_u32(&M.vfull[s]));
-            const int64_t u_prev = u;
-            adv2(u, ti);
-            if (u != u_prev && j + 2 < n) wscale = unit_wscale(P.p.nmax[u / P.nrg]);
-        }
-        cp_async_wait<0>();   // no copy may land in shared memory after the CTA exits
-    } else if (warp < 8 + kSmWarps) {
-        // =============================== softmax + epilogue (four groups of 16 rows)
-        const int grp = (warp - 8) >> 2;        // row group: rows 16*grp .. 16*grp+15
-        const int wq = warp & 3;                // TMEM lane quadrant
-        const int tt = wq * 32 + lane;          // token slot = TMEM lane (= head-dim index in the epilogue)
-        const int si = tid - 256;               // 0 .. kSmThreads-1 over all groups
-        const uint32_t lane_addr = tbase + ((uint32_t)(wq * 32) << 16);
-        const uint32_t gbar = kBarGroup + grp;
-        int R = 0;                               // rows of the current segment
-        const int rbase = kGRows * grp;
-        int seg = -1;
-        int64_t seg_u = -1;
-        int64_t u = g0 / nt;
-        int ti = (int)(g0 - u * nt) - 1;
-        for (int j = 0; j < n; ++j) {
-            if (++ti == nt) {
-                ti = 0;
-                ++u;
-            }
-            const int s = j & 1;
-            const uint32_t ph = (uint32_t)((j >> 1) & 1);
-            const bool first = (j == 0) || (ti == 0);
-            const bool last = (j == n - 1) || (ti == nt - 1);
-            if (first) {
-                ++seg;
-                seg_u = u;
-                const int rg = (int)(u % P.nrg);
-                R = min(kNR, P.Rtot - kNR * rg);
-                softmax_prologue<QBF16>(P.q, P.p.nmax, u / P.nrg, kNR * rg, P.p.H, P.A, P.Hq, P.G, R, P.scale_log2, sQ,
-                                        M, si, warp - 8, lane);
-                // the next segment's query rows go to L2 now, so its prologue does not wait on HBM
-                const int64_t un = u + 1;
-                if (un < (g1 + nt - 1) / nt && si < kNR * 2) {
-                    const int rgn = (int)(un % P.nrg);
-                    const int rn = kNR * rgn + (si >> 1);          // two threads per row, 128 B each
-                    if (rn < P.Rtot && (si >> 1) < kNR) {
-                        const int64_t pun = un / P.nrg;
-                        const int layer = (int)(pun / P.p.H), kvh = (int)(pun % P.p.H);
-                        const uint16_t* qa = P.q + (((int64_t)layer * P.A + rn / P.G) * P.Hq + kvh * P.G + rn % P.G) * kD +
-                                             (si & 1) * 64;
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(qa));
-                    }
-                }
-            }
-            const float scale_eff = M.scale_eff;
-            const bool tail = (int64_t)(ti + 1) * kTile > P.n_ctx;
-            const bool valid = (int64_t)ti * kTile + tt < P.n_ctx;
-            // -------- logits for this group's 16 rows, d = c * S - m (absolute c * S on a segment's
-            // first tile, before the running max exists). S and the per-slot row sums come from TMEM in
-            // one round trip and stay in registers; if a new running max is needed (the segment's first
-            // tile, or a logit above the max by more than 2^tau) the max is updated and the tile is
-            // read again against it, so no tile data is live across the out-of-line update.
-            const float2 c2 = make_float2(scale_eff, scale_eff);
-            tc::mbar_wait(tc::smem_u32(&M.sfull[s]), ph, abortp, kTimeoutNs);
-            tc::fence_after();
-            if (j >= 2) tc::mbar_wait(tc::smem_u32(&M.pvfree[s]), ph ^ 1u, abortp, kTimeoutNs);
-            uint32_t sd[16], ls[16];   // S, then d, as float bits; per-slot row sums
-            bool absolute = first;
-            for (;;) {
-                tc::tmem_ld16(lane_addr + kColS + 64u * s + rbase, sd);
-                if (!first) tc::tmem_ld16(lane_addr + kColL + rbase, ls);
-                tc::wait_ld();
-                if (first) {   // a segment starts its row sums at zero
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) ls[k] = 0u;
-                }
-                const float2* nm2 = reinterpret_cast<const float2*>(&M.nm[rbase]);
-                float dmax = -INFINITY;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 sv = make_float2(__uint_as_float(sd[2 * k]), __uint_as_float(sd[2 * k + 1]));
-                    float2 d = absolute ? mul2(c2, sv) : fma2(c2, sv, nm2[k]);
-                    if (tail && !valid) d = make_float2(-INFINITY, -INFINITY);
-                    dmax = fmaxf(dmax, fmaxf(d.x, d.y));
-                    sd[2 * k] = __float_as_uint(d.x);
-                    sd[2 * k + 1] = __float_as_uint(d.y);
-                }
-                const bool need = absolute || bar_any(kBarRed + grp, 128, dmax > kTau);
-                if (!need) break;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float v0 = tc::warp_max(__uint_as_float(sd[2 * k]));
-                    const float v1 = tc::warp_max(__uint_as_float(sd[2 * k + 1]));
-                    if (lane == 2 * k) M.red[grp][wq][2 * k] = v0;
-                    if (lane == 2 * k + 1) M.red[grp][wq][2 * k + 1] = v1;
-                }
-                softmax_new_max(M, grp, tt, rbase, R, gbar, absolute, j, lane_addr, abortp);
-                absolute = false;   // the second pass sees every logit at or below the new max
-            }
-            // -------- probabilities p = 2^d (fp16) and running sums
-            const uint32_t prow = tc::smem_u32(sP) + s * 16384;
-#pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) {   // 8 rows per 16-byte chunk
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int k = 4 * c8 + e;
-                    const float p0 = ex2(__uint_as_float(sd[2 * k])), p1 = ex2(__uint_as_float(sd[2 * k + 1]));
-                    const __half2 h = __floats2half2_rn(p0, p1);
-                    pk[e] = *reinterpret_cast<const uint32_t*>(&h);
-                    const float2 l =
-                        add2(make_float2(__uint_as_float(ls[2 * k]), __uint_as_float(ls[2 * k + 1])), make_float2(p0, p1));
-                    ls[2 * k] = __float_as_uint(l.x);
-                    ls[2 * k + 1] = __float_as_uint(l.y);
-                }
-                st_shared16(prow + tc::sw128((uint32_t)tt, 16u * (2 * grp + c8)), pk[0], pk[1], pk[2], pk[3]);
-            }
-            tc::tmem_st16(lane_addr + kColL + rbase, ls);
-            tc::fence_before();
-            tc::mbar_arrive(tc::smem_u32(&M.sfree[s]));   // S has been read for the last time
-            tc::fence_proxy_async();
-            tc::mbar_arrive(tc::smem_u32(&M.pfull[s]));
-
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.pvfull));
+            // -- g. end of a segment piece: its (m, l) now, its O after MMA2(i) (next tile or below)
             if (last) {
-                // one partial per (segment, CTA): slot = segment + CTA (distinct, at most segments + CTAs)
-                softmax_epilogue(M, s, ph, abortp, lane_addr, grp, wq, lane, tt, rbase, R, P.RS, gbar, seg_u + c,
-                                 P.ws_acc, P.ws_ml);
+                const int64_t slot = cur.seg + cta;   // one partial per (segment, CTA): distinct
+                write_row_stats(l, M, g, qd, lane, R, P.ws_ml + slot * P.RS * 2);
+                epi = true;
+                epi_R = R;
+                epi_inv_w = 1.0f / wsc;
+                epi_slot = slot;
+            }
+            // -- h. queries of tile i+2's segment (its buffer was last used by the segment before
+            //       tile i+1's, whose MMA1s have all completed)
+            if (qprep) {
+                const int qb = (int)((c2.seg - seg0) & 1);
+                q_store<QBF16>(qr, sm_u + kSmQ + (uint32_t)qb * 16384u, M, qb, g, qd, lane, P.scale_log2);
+            }
+            cur = c1;
+            c1 = c2;
+            c2.adv(nt, nrg);
+        }
+        if (epi) {
+            tc::mbar_wait(tc::smem_u32(&M.mma2done), (uint32_t)((n - 1) & 1), abortp, kTimeoutNs);
+            tc::fence_after();
+            uint32_t ov[16];
+            tc::tmem_ld16(lane_addr + kColO + 16u * g, ov);
+            tc::wait_ld();
+            float* acc = P.ws_acc + epi_slot * P.RS * kD;
+#pragma unroll
+            for (int k = 0; k < kGRows; ++k) {
+                const int r = kGRows * g + k;
+                if (r < epi_R) acc[r * kD + t] = __uint_as_float(ov[k]) * epi_inv_w;
             }
         }
-    } else if (warp == kWarpMma) {
-        // =============================== MMA issuer: an event loop over both chains
-        // The whole warp runs the loop with warp-uniform control (barrier tests broadcast from lane
-        // 0) and one elected lane issues the MMAs and commits. Issuing from a converged warp instead
-        // of a single-lane branch cut the tile period by about a tenth.
-        const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);
-        const uint32_t id2 = tc::idesc_f16(128, kNR, true, true);
-        // Shared-memory descriptors, built once: the start-address field holds address >> 4, so a
-        // k-step or stage offset is added to the descriptor itself (every operand is below 256 KB).
-        // The issuing warp shares its SM sub-partition with six other warps; every instruction it
-        // saves per MMA shortens the tile.
-        const bool leader = tc::elect_one();
-        uint64_t bq[8];
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) bq[ks] = tc::sdesc(tc::smem_u32(sQ) + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024);
-        const uint64_t av0 = tc::sdesc(tc::smem_u32(sV), 16384, 1024);
-        const uint64_t bp0 = tc::sdesc(tc::smem_u32(sP), 16384, 1024);
-        const uint32_t tS = tbase + kColS, tK = tbase + kColK, tO = tbase + kColO;
-        int j1 = 0, j2 = 0;        // next MMA1 / MMA2 tile
-        int seg1 = 0;              // segments whose first MMA1 has been issued
-        int ti1 = (int)(g0 % nt), ti2 = ti1;
-        bool ok = P.test_stall == 0;
-        uint64_t t_last = tc::globaltimer();
-        while (ok && j2 < n) {
-            bool prog = false;
-            if (j1 < n) {
-                const int s = j1 & 1;
-                const bool f1 = (j1 == 0) || (ti1 == 0);
-                const bool r1 = (!f1 || tc::mbar_test(tc::smem_u32(&M.qready), (uint32_t)(seg1 & 1))) &&
-                                tc::mbar_test(tc::smem_u32(&M.kfull[s]), (uint32_t)((j1 >> 1) & 1)) &&
-                                (j1 < 2 || tc::mbar_test(tc::smem_u32(&M.sfree[s]), (uint32_t)(((j1 - 2) >> 1) & 1)));
-                if (__shfl_sync(0xffffffffu, r1 ? 1 : 0, 0)) {
+        tc::fence_before();
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther));
+        if (warp == kWarpMma) {
+            // =========================== MMA issuer: the warp runs the loop converged; one elected
+            // lane issues each tile's eight MMAs and its commit from a single asm statement
+            const uint32_t id1 = tc::idesc_f16(128, kNR, false, false);   // A (keys) in TMEM, B (queries) K-major
+            const uint32_t id2 = tc::idesc_f16(128, kNR, false, true);    // A (values) in TMEM, B (P') MN-major
+            const uint64_t bq0 = tc::sdesc(sm_u + kSmQ, 16, 1024);
+            const uint64_t bp0 = tc::sdesc(sm_u + kSmP, 16384, 1024);
+            const uint32_t tS = tbase + kColS, tK = tbase + kColK, tV = tbase + kColV, tO = tbase + kColO;
+            const uint32_t b_sfull = tc::smem_u32(&M.sfull), b_m2 = tc::smem_u32(&M.mma2done);
+            // bounded wait by lane 0, result broadcast so that the warp stays converged
+            auto wait0 = [&](uint64_t& bar, uint32_t ph) -> bool {
+                int ok = 1;
+                if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&bar), ph, abortp, kTimeoutNs) ? 1 : 0;
+                return __shfl_sync(0xffffffffu, ok, 0) != 0;
+            };
+            const int64_t seg0 = c0.seg;
+            int ti = c0.ti;
+            int64_t seg = c0.seg;
+            bool prev_first = true;
+            int issued = 0;
+            bool ok = P.test_stall == 0;
+            for (int i = 0; i <= n && ok; ++i) {
+                bool cur_first = false;
+                if (i < n) {
+                    cur_first = (i == 0) || (ti == 0);
+                    const int64_t k = seg - seg0;
+                    ok = wait0(M.kfull[i & 1], (uint32_t)((i >> 1) & 1));
+                    if (ok && i > 0) ok = wait0(M.sfree, (uint32_t)((i - 1) & 1));
+                    if (ok && cur_first) ok = wait0(M.qready[k & 1], (uint32_t)((k >> 1) & 1));
+                    if (!ok) break;
                     tc::fence_after();
-                    const uint32_t dS = tS + 64u * s, aK = tK + 128u * s;
-                    if (leader) {
-                        tc::mma_ts_c<0>(dS, aK, bq[0], id1);   // hi then lo halves of the scaled keys
-#pragma unroll
-                        for (int ks = 1; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 8u * ks, bq[ks], id1);
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) tc::mma_ts_c<1>(dS, aK + 64u + 8u * ks, bq[ks], id1);
-                        tc::commit(tc::smem_u32(&M.sfull[s]));
-                        tc::commit(tc::smem_u32(&M.kfree[s]));
-                    }
-                    if (f1) ++seg1;
-                    if (++ti1 == nt) ti1 = 0;
-                    ++j1;
-                    prog = true;
+                    issue_mma1(tS, tK + (uint32_t)(i & 1) * 64u, bq0 + (uint64_t)((k & 1) * (16384 >> 4)), id1, b_sfull);
+                    issued = 1;
+                }
+                if (i > 0) {
+                    ok = wait0(M.pvfull, (uint32_t)((i - 1) & 1));
+                    if (!ok) break;
+                    tc::fence_after();
+                    issue_mma2(tO, tV, bp0 + (uint64_t)(((i - 1) & 1) * (16384 >> 4)), id2, prev_first ? 1u : 0u, b_m2);
+                }
+                __syncwarp();
+                prev_first = cur_first;
+                if (i < n && ++ti == nt) {
+                    ti = 0;
+                    ++seg;
                 }
             }
-            if (j2 < j1) {
-                const int s2 = j2 & 1;
-                const uint32_t ph2 = (uint32_t)((j2 >> 1) & 1);
-                const bool r2 = tc::mbar_test(tc::smem_u32(&M.vfull[s2]), ph2) && tc::mbar_test(tc::smem_u32(&M.pfull[s2]), ph2);
-                if (__shfl_sync(0xffffffffu, r2 ? 1 : 0, 0)) {
-                    const bool f2 = (j2 == 0) || (ti2 == 0);
-                    tc::fence_after();
-                    const uint64_t ad = av0 + (uint64_t)(s2 * (32768 >> 4));
-                    const uint64_t bd = bp0 + (uint64_t)(s2 * (16384 >> 4));
-                    if (leader) {
-                        if (f2)
-                            tc::mma_ss_c<0>(tO, ad, bd, id2);
-                        else
-                            tc::mma_ss_c<1>(tO, ad, bd, id2);
-#pragma unroll
-                        for (int ks = 1; ks < 8; ++ks)
-                            tc::mma_ss_c<1>(tO, ad + (uint64_t)(ks * (2048 >> 4)), bd + (uint64_t)(ks * (2048 >> 4)), id2);
-                        tc::commit(tc::smem_u32(&M.pvfree[s2]));
-                    }
-                    if (++ti2 == nt) ti2 = 0;
-                    ++j2;
-                    prog = true;
+            if (P.test_stall) *abortp = 0;   // let the workers discover the stall on their own waits
+            if (issued) {
+                // every MMA this warp issued must have completed before the TMEM is freed
+                commit_elected(tc::smem_u32(&M.done));
+                int fin = 1;
+                if (lane == 0) {
+                    volatile int dummy = 0;
+                    fin = tc::mbar_wait(tc::smem_u32(&M.done), 0u, &dummy, 50000000ull) ? 1 : 0;
+                    if (!fin) *abortp = 1;   // reported through the pool's status word
                 }
+                __syncwarp();
             }
-            if (prog) {
-                t_last = tc::globaltimer();
-            } else {
-                // lane 0 decides, so the warp leaves the loop together
-                const int stop = *abortp ? 1 : (tc::globaltimer() - t_last > kTimeoutNs ? 2 : 0);
-                const int stop0 = __shfl_sync(0xffffffffu, stop, 0);
-                if (stop0 == 2 && lane == 0) *abortp = 1;
-                if (stop0) break;
+        } else if (warp == kWarpTma && lane == 0) {
+            // =========================== producer: each tile's key codes (2-D tensor copy, 128-byte
+            // swizzle), value codes, scales and norms (1-D bulk copies) into the ring
+            Cursor c = c0;
+            int issued = 0;
+            for (int j = 0; j < n && !*abortp; ++j) {
+                const int st = j % kStages;
+                if (j >= kStages &&
+                    !tc::mbar_wait(tc::smem_u32(&M.rempty[st]), (uint32_t)(((j / kStages) - 1) & 1), abortp, kTimeoutNs))
+                    break;
+                const int64_t row = c.unit * P.p.cap + (int64_t)c.ti * kTile;   // pool row of token 0
+                const uint32_t dst = sm_u + kSmRing + (uint32_t)st * kStageBytes;
+                const uint32_t bar = tc::smem_u32(&M.rfull[st]);
+                tc::mbar_arrive_expect_tx(bar, kStageTx);
+                tc::tma_2d_g2s(dst + kStKeys, &P.kmap, 0, (int32_t)row, bar);
+                tc::bulk_g2s(dst + kStVals, P.p.vc + row * (3 * kD / 8), kTile * 3 * kD / 8, bar);
+                tc::bulk_g2s(dst + kStScales, P.p.ks + row * (kD / kQ8Block), kTile * (kD / kQ8Block) * 2, bar);
+                tc::bulk_g2s(dst + kStNorms, P.p.vn + row, kTile * 2, bar);
+                issued = j + 1;
+                c.adv(nt, nrg);
             }
-        }
-        if (P.test_stall) *abortp = 0;  // let the other roles discover the stall on their own waits
-        if (j1 > 0) {
-            // every MMA this warp issued must have completed before the TMEM is freed
-            if (leader) tc::commit(tc::smem_u32(&M.done));
-            volatile int dummy = 0;
-            tc::mbar_wait(tc::smem_u32(&M.done), 0u, &dummy, 50000000ull);
+            // drain: no copy may land in shared memory after the CTA has exited
+            for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+                volatile int dummy = 0;
+                tc::mbar_wait(tc::smem_u32(&M.rfull[j % kStages]), (uint32_t)((j / kStages) & 1), &dummy, 50000000ull);
+            }
         }
     }
 
     // ---- tear-down: every role is past its last TMEM access
-    tc::fence_before();
     __syncthreads();
     if (warp == kWarpMma) {
         tc::fence_after();
@@ -850,16 +893,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (tid == 0 && M.abort) atomicOr(P.p.status, 1u);
 }
 
-int g_num_sms = 0;
-
+// SM count of the current device (read per call: cheap, and right for every device of a process)
 int num_sms() {
-    if (g_num_sms == 0) {
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
-        g_num_sms = v;
-    }
-    return g_num_sms;
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    return v;
 }
 
 struct TcPlan {
@@ -881,6 +920,38 @@ TcPlan plan(const PoolView& p, int rows, int64_t n_ctx) {
     return pl;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once (no link-time dependency on libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The pool's key codes as a 2-D uint8 tensor [U * cap rows][128 B] read in 128 x 128 boxes with the
+// 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8)).
+polykv_status key_tensor_map(const PoolView& p, CUtensorMap* m) {
+    const int64_t rows = (int64_t)p.L * p.H * p.cap;
+    if (rows >= ((int64_t)1 << 31)) return set_error(POLYKV_E_UNSUPPORTED, "attend_tc: pool too large (%lld rows)", (long long)rows);
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return set_error(POLYKV_E_CUDA, "attend_tc: cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kTile};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)p.kq, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(POLYKV_E_CUDA, "attend_tc: tensor map encode failed (%d)", (int)r);
+    return POLYKV_OK;
+}
+
 }  // namespace
 
 bool attend_tc_supported(const PoolView& p, int rows) { return p.d == kD && rows >= 1; }
@@ -899,7 +970,10 @@ polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q
     const TcPlan pl = plan(p, R, n_ctx);
     const size_t need = attend_tc_workspace(p, R, n_ctx);
     if (ws_bytes < need) return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend: workspace %zu < %zu bytes", ws_bytes, need);
+    if (pl.nt > 0x7FFFFFFF) return set_error(POLYKV_E_UNSUPPORTED, "attend: context too long");
     TcParams P;
+    const polykv_status ms = key_tensor_map(p, &P.kmap);
+    if (ms != POLYKV_OK) return ms;
     P.p = p;
     P.q = static_cast<const uint16_t*>(q);
     P.ws_acc = static_cast<float*>(ws);

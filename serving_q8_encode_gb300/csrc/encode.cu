@@ -4,10 +4,14 @@
 // for Multi-Agent LLM Inference"): keys int8 q8_0, values FWHT rotation then
 // 3-bit Lloyd-Max quantization tuned to N(0,1), written once.
 //
-// Work mapping: d/32 lanes own one (layer, kv head, token) position; each lane
-// holds one whole 32-element q8_0 block of the key and 32 consecutive value
-// coordinates (four 16-byte loads each). The fp32 operation order is fixed
-// (the CPU oracle restates it):
+// Work mapping: one block of d threads per (unit, group of 32 consecutive pool
+// tokens). Phase 1: d/32 lanes own one token; each lane holds one whole
+// 32-element q8_0 block of the key and 32 consecutive value coordinates (four
+// 16-byte loads each), writes the key codes and scale, and leaves the rotated
+// value coordinates in shared memory. Phase 2: thread j decides the 32 tokens'
+// codes of coordinate j and writes them as the pool's 12-byte string (token k
+// at bits 3k..3k+2). The fp32 operation order is fixed (the CPU oracle
+// restates it):
 //   keys:   amax over the block; s16 = fp16_rn(amax / 127) (IEEE division);
 //           code = round-half-away(x / s16), the quotient correctly rounded;
 //   values: ||v||^2 = per 8-coordinate group a left-to-right sum of rounded
@@ -135,18 +139,43 @@ __device__ __forceinline__ uint32_t bytes4(int a, int b, int c, int d) {
     return w;
 }
 
+// One block of D threads per (unit, 32-token group) inside [t0, t0 + n). Phase 1: d/32 lanes per
+// token (token tau = lane group, quarter gl) do the keys and the value norm + FWHT as before and
+// leave the rotated coordinates y in shared memory. Phase 2: thread j = coordinate j takes the 32
+// tokens' y_j, decides their 3-bit codes and packs them into the coordinate's 12-byte string
+// (token k at bits 3k..3k+2). Tokens of a partly covered group that lie outside [t0, t0 + n) keep
+// the bits already in the pool.
+template <int D>
+struct EncSmem {
+    static constexpr int kRow = D + 4;   // padded row of y (floats); chunks rotated, see enc_phys
+    float y[32][kRow];
+    float4 th[32];                       // per token: boundaries b4..b6 times ||v|| (+inf when ||v|| = 0)
+};
+
+// physical float index of coordinate j inside a row of EncSmem::y: 16-byte chunk c of lane quarter gl
+// is stored at chunk (c + (256 / D) gl) mod 8 of that quarter; with the 4-float row padding, the
+// lanes of one 8-lane store phase (8 / (D / 32) tokens x D / 32 quarters) land on distinct banks
+template <int D>
+__device__ __forceinline__ int enc_phys(int j) {
+    const int gl = j >> 5, c = (j >> 2) & 7;
+    return (gl << 5) | (((c + (256 / D) * gl) & 7) << 2) | (j & 3);
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256, 4) encode_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
-                                                     PoolView p, int64_t n_tok, int64_t t0, int64_t n_vec) {
-    constexpr int LPV = D / 32;          // lanes per vector
-    constexpr int VPB = 256 / LPV;       // vectors per block
-    const int gl = threadIdx.x % LPV;
-    const int vloc = threadIdx.x / LPV;
-    const int64_t vi_raw = (int64_t)blockIdx.x * VPB + vloc;
-    const bool valid = vi_raw < n_vec;
-    const int64_t vi = valid ? vi_raw : n_vec - 1;   // every lane takes part in the shuffles
-    const int64_t unit = n_vec <= 0xFFFFFFFFll ? (int64_t)((uint32_t)vi / (uint32_t)n_tok) : vi / n_tok;
-    const int64_t pidx = unit * p.cap + t0 + (vi - unit * n_tok);
+__global__ void __launch_bounds__(D, D == 128 ? 8 : 12) encode_kernel(const uint16_t* __restrict__ k,
+                                                           const uint16_t* __restrict__ v, PoolView p,
+                                                           int64_t n_tok, int64_t t0, int g_first, int n_groups) {
+    constexpr int LPV = D / 32;          // lanes per token in phase 1
+    __shared__ EncSmem<D> sm;
+    const int tid = threadIdx.x;
+    const int gl = tid % LPV;
+    const int tau = tid / LPV;           // token of the group, 0..31
+    const int64_t unit = blockIdx.x / n_groups;
+    const int64_t grp = g_first + (int64_t)(blockIdx.x % n_groups);
+    const int64_t tk = grp * 32 + tau;   // pool token
+    const bool valid = tk >= t0 && tk < t0 + n_tok;
+    const int64_t vi = unit * n_tok + (valid ? tk - t0 : 0);   // input row (row 0 of the unit if not valid)
+    const int64_t pidx = unit * p.cap + tk;
 
     // both 64-byte rows are requested before any arithmetic (one memory round trip per lane)
     uint4 kraw[4], vraw[4];
@@ -204,7 +233,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(const uint16_t* __restri
         }
     }
 
-    // ---------------- values: norm, FWHT, 3-bit codes
+    // ---------------- values, phase 1: norm and FWHT of this lane's quarter
     float y[32];
     unpack32(vraw, y, BF16);
     float nrm;
@@ -263,55 +292,90 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(const uint16_t* __restri
             y[i + 1] = r.y;
         }
     }
-    // boundaries scaled by the norm (positive ones; the negative ones mirror them)
-    const float t4 = __fmul_rn(kB4, nrm);
-    const float t5 = __fmul_rn(kB5, nrm);
-    const float t6 = __fmul_rn(kB6, nrm);
-    // eight codes c_0..c_7 -> the 24-bit group sum c_i * 8^i, formed exactly in fp32: Horner over the
-    // half-codes h_i = c_i - 3.5 gives sum h_i 8^i, a multiple of 1/2 below 2^23 in magnitude (24
-    // significant bits at most, so every step is exact); adding 3.5 * sum 8^i = 8388607.5 gives the
-    // integer group sum (< 2^24), also exactly
-    uint32_t w24[4];
+    // the rotated coordinates go to shared memory (rotated chunks, see enc_phys), with the token's
+    // norm-scaled boundaries; a zero norm gets infinite thresholds, so every code is 4 (u = 0)
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        float w = value_half_code(y[8 * g + 7], t4, t5, t6);
-#pragma unroll
-        for (int i = 6; i >= 0; --i) w = fmaf(w, 8.0f, value_half_code(y[8 * g + i], t4, t5, t6));
-        w24[g] = (uint32_t)__float2uint_rz(w + 8388607.5f);
+    for (int c = 0; c < 8; ++c) {
+        float4* dst = reinterpret_cast<float4*>(&sm.y[tau][enc_phys<D>(32 * gl + 4 * c)]);
+        *dst = make_float4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
     }
-    if (!(nrm > 0.0f)) {   // ||v|| = 0: u = 0 everywhere, code 4
-#pragma unroll
-        for (int g = 0; g < 4; ++g) w24[g] = 0x924924u;
-    }
-    if (valid) {
-        // this lane's 32 codes are bits 96*gl .. 96*gl+95 of the vector's packed row
-        uint32_t* dst = reinterpret_cast<uint32_t*>(p.vc + pidx * (3 * D / 8) + gl * 12);
-        dst[0] = w24[0] | (w24[1] << 24);
-        dst[1] = (w24[1] >> 8) | (w24[2] << 16);
-        dst[2] = (w24[2] >> 16) | (w24[3] << 8);
-        if (gl == 0) p.vn[pidx] = __float2half_rn(nrm);
+    if (gl == 0) {
+        const bool pos = nrm > 0.0f;
+        sm.th[tau] = pos ? make_float4(__fmul_rn(kB4, nrm), __fmul_rn(kB5, nrm), __fmul_rn(kB6, nrm), 0.0f)
+                         : make_float4(INFINITY, INFINITY, INFINITY, 0.0f);
+        if (valid) p.vn[pidx] = __float2half_rn(nrm);
     }
     // running per-unit maximum of ||v|| (an upper bound used by attention to scale fp16 operands):
-    // one max-reduction per warp and one atomic when the warp's vectors share a unit (the common
-    // case), else one atomic per vector. Norms are non-negative, so their bit patterns order as uints.
-    const uint32_t nb = (gl == 0 && valid) ? __float_as_uint(nrm) : 0u;
-    const int64_t unit0 = __shfl_sync(0xffffffffu, unit, 0);
-    if (__all_sync(0xffffffffu, unit == unit0)) {
+    // one max-reduction per warp, one atomic per warp. Norms are non-negative, so their bit patterns
+    // order as unsigned integers.
+    {
+        const uint32_t nb = (gl == 0 && valid) ? __float_as_uint(nrm) : 0u;
         const uint32_t mx = __reduce_max_sync(0xffffffffu, nb);
-        if ((threadIdx.x & 31) == 0 && mx != 0u) atomicMax(reinterpret_cast<unsigned int*>(p.nmax) + unit0, mx);
-    } else if (gl == 0 && valid && nb != 0u) {
-        atomicMax(reinterpret_cast<unsigned int*>(p.nmax) + unit, nb);
+        if ((tid & 31) == 0 && mx != 0u) atomicMax(reinterpret_cast<unsigned int*>(p.nmax) + unit, mx);
+    }
+    __syncthreads();
+
+    // ---------------- values, phase 2: thread j = coordinate j packs the group's 32 codes
+    {
+        const int j = tid;
+        const int pj = enc_phys<D>(j);
+        const int64_t g0tok = grp * 32;
+        const int kmin = (int)(t0 > g0tok ? t0 - g0tok : 0);                    // valid tokens: [kmin, kmax)
+        const int kmax = (int)(t0 + n_tok - g0tok < 32 ? t0 + n_tok - g0tok : 32);
+        // eight codes c_0..c_7 -> the 24-bit group sum c_i * 8^i, formed exactly in fp32: Horner over
+        // the half-codes h_i = c_i - 3.5 gives sum h_i 8^i, a multiple of 1/2 below 2^23 in magnitude
+        // (24 significant bits at most, so every step is exact); adding 3.5 * sum 8^i = 8388607.5
+        // gives the integer group sum (< 2^24), also exactly. A token outside [t0, t0 + n) gets the
+        // half-code -3.5 (code 0) and its bits are taken from the pool below.
+        uint32_t w24[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float w = 0.0f;
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                const int kk = 8 * g + i;
+                const float4 th = sm.th[kk];
+                float h = value_half_code(sm.y[kk][pj], th.x, th.y, th.z);
+                if (kk < kmin || kk >= kmax) h = -3.5f;
+                w = (i == 7) ? h : fmaf(w, 8.0f, h);
+            }
+            w24[g] = (uint32_t)__float2uint_rz(w + 8388607.5f);
+        }
+        uint32_t o0 = w24[0] | (w24[1] << 24);
+        uint32_t o1 = (w24[1] >> 8) | (w24[2] << 16);
+        uint32_t o2 = (w24[2] >> 16) | (w24[3] << 8);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.vc + ((unit * (p.cap / 32) + grp) * D + j) * 12);
+        if (kmin > 0 || kmax < 32) {
+            // a partly covered group keeps the other tokens' bits already in the pool
+            const int lo = 3 * kmin, hi = 3 * kmax;   // new bits: [lo, hi) of the 96-bit string
+            auto span = [](int a, int b) -> uint32_t {   // bits [a, b) of one 32-bit word, a, b clamped
+                a = a < 0 ? 0 : (a > 32 ? 32 : a);
+                b = b < 0 ? 0 : (b > 32 ? 32 : b);
+                const uint32_t up = b >= 32 ? 0xFFFFFFFFu : ((1u << b) - 1u);
+                const uint32_t dn = a >= 32 ? 0xFFFFFFFFu : ((1u << a) - 1u);
+                return up & ~dn;
+            };
+            const uint32_t m0 = span(lo, hi), m1 = span(lo - 32, hi - 32), m2 = span(lo - 64, hi - 64);
+            o0 = (dst[0] & ~m0) | (o0 & m0);
+            o1 = (dst[1] & ~m1) | (o1 & m1);
+            o2 = (dst[2] & ~m2) | (o2 & m2);
+        }
+        dst[0] = o0;
+        dst[1] = o1;
+        dst[2] = o2;
     }
 }
 
 template <int D, bool BF16>
 polykv_status run(const PoolView& p, const void* k, const void* v, int64_t t0, int64_t n, cudaStream_t st) {
-    const int64_t n_vec = (int64_t)p.L * p.H * n;
-    constexpr int VPB = 256 / (D / 32);
-    const int64_t blocks = (n_vec + VPB - 1) / VPB;
-    if (blocks > 0x7FFFFFFF) return set_error(POLYKV_E_UNSUPPORTED, "encode: too many vectors (%lld)", (long long)n_vec);
-    encode_kernel<D, BF16><<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(k),
-                                                              static_cast<const uint16_t*>(v), p, n, t0, n_vec);
+    const int64_t g_first = t0 / 32, g_last = (t0 + n - 1) / 32;
+    const int64_t n_groups = g_last - g_first + 1;
+    const int64_t blocks = (int64_t)p.L * p.H * n_groups;
+    if (blocks > 0x7FFFFFFF || g_last > 0x7FFFFFFF)
+        return set_error(POLYKV_E_UNSUPPORTED, "encode: too many token groups (%lld)", (long long)blocks);
+    encode_kernel<D, BF16><<<(unsigned)blocks, D, 0, st>>>(static_cast<const uint16_t*>(k),
+                                                           static_cast<const uint16_t*>(v), p, n, t0, (int)g_first,
+                                                           (int)n_groups);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "encode launch: %s", cudaGetErrorString(e));
     return POLYKV_OK;

@@ -37,7 +37,8 @@ def check_encode(pool, ref, n_tok, t_off=0, b32=None):
     assert np.array_equal(f["k_codes"][:, :, sl], ref["k_codes"]), "q8 codes differ"
     assert np.array_equal(f["k_scales"][:, :, sl].view(np.uint16), ref["k_scales"].view(np.uint16)), "scales differ"
     assert np.array_equal(f["v_norms"][:, :, sl].view(np.uint16), ref["v_norms"].view(np.uint16)), "norms differ"
-    got = oracle.values.unpack_codes(f["v_packed"][:, :, sl], ref["v_codes"].shape[-1])
+    d = ref["v_codes"].shape[-1]
+    got = oracle.values.unpack_codes(f["v_packed"], d)[:, :, sl]
     diff = got != ref["v_codes"]
     if diff.any():
         u = ref["u"][diff].astype(np.float64)
@@ -45,8 +46,10 @@ def check_encode(pool, ref, n_tok, t_off=0, b32=None):
                       np.maximum(np.abs(b32.astype(np.float64)), 1.0)[None, :], axis=1)
         assert np.all(dist <= 1e-6), f"{int(diff.sum())} code mismatches away from a boundary"
         assert diff.sum() <= max(1, 1e-5 * diff.size)
-    else:
-        assert np.array_equal(f["v_packed"][:, :, sl], ref["v_packed"])
+    elif t_off % 32 == 0 and n_tok >= 32:
+        # whole 32-token groups: the packed bytes themselves
+        ng = n_tok // 32
+        assert np.array_equal(f["v_packed"][:, :, t_off // 32:t_off // 32 + ng], ref["v_packed"][:, :, :ng])
 
 
 @pytest.fixture(params=["default", "simt"])
@@ -230,7 +233,7 @@ def test_non_finite_key_blocks(env):
     pool.encode(_dev(torch, kb), _dev(torch, vb))
     torch.cuda.synchronize()
     ref = oracle.attention.encode_pool(kb, vb, "bf16", b32)
-    f = {n: x.cpu().numpy()[:, :, :T] for n, x in pool.fields().items()}
+    f = {n: x.cpu().numpy()[:, :, :T] for n, x in pool.fields().items() if n != "v_packed"}
     for (t, blk) in ((2, 1), (5, 3), (6, 0)):
         assert not np.isfinite(ref["k_scales"][0, 0, t, blk]) and not np.isfinite(f["k_scales"][0, 0, t, blk])
         assert np.isnan(ref["k_scales"][0, 0, t, blk]) == np.isnan(f["k_scales"][0, 0, t, blk])
@@ -238,7 +241,8 @@ def test_non_finite_key_blocks(env):
     fin = np.isfinite(ref["k_scales"])
     assert np.array_equal(f["k_scales"][fin].view(np.uint16), ref["k_scales"][fin].view(np.uint16))
     assert np.array_equal(f["k_codes"], ref["k_codes"])
-    assert np.array_equal(f["v_packed"], ref["v_packed"])
+    got_codes = oracle.values.unpack_codes(pool.fields()["v_packed"].cpu().numpy(), d)[:, :, :T]
+    assert np.array_equal(got_codes, ref["v_codes"])
     assert np.array_equal(f["v_norms"].view(np.uint16), ref["v_norms"].view(np.uint16))
 
 
