@@ -146,7 +146,7 @@ struct Misc {
     float qc[2][kGroups];              // per query buffer and row group: logit scale / query scale
     int abort;
     int pad;
-    uint64_t sfull, sfree, kfull[2], pvfull, mma2done, qready[2], done;
+    uint64_t sfull, kready, pvfull, mma2done, qready[2], done;   // kready: next key operand in TMEM + S read
     uint64_t rfull[kStages], rempty[kStages];
     uint32_t tslot;
 };
@@ -419,7 +419,8 @@ __device__ __forceinline__ void q_store(const uint4 (&raw)[2], uint32_t qbuf_u, 
 }
 
 // Row sums of this row group over the 128 token slots (lanes x quadrants) at the end of a segment
-// piece, written with the rows' running maxima as the piece's (m, l) partial.
+// piece, written with the rows' running maxima as the piece's (m, l) partial; the rows' logit
+// addends are reset for the next segment.
 __device__ __forceinline__ void write_row_stats(const float2 (&l)[8], Misc& M, int g, int qd, int lane, int R,
                                                 float* __restrict__ ml_slot) {
     float v[16];
@@ -455,6 +456,9 @@ __device__ __forceinline__ void write_row_stats(const float2 (&l)[8], Misc& M, i
     v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
     const int row = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
     if ((lane & 1) == 0) M.red[g][qd][row] = v[0];
+    // the next segment's first tile takes absolute logits (its addend -m reads 0); every thread of the
+    // group has read this tile's addends before the tile's OR barrier
+    if (qd == 1 && lane < kGRows) M.nm[kGRows * g + lane] = 0.0f;
     tc::named_bar(kBarGroup + g, 128);
     if (qd == 0 && lane < kGRows) {
         const int r = kGRows * g + lane;
@@ -491,9 +495,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
     // ---- set-up: barriers, centroid-pair table, TMEM
     if (tid == 0) {
         tc::mbar_init(tc::smem_u32(&M.sfull), 1);
-        tc::mbar_init(tc::smem_u32(&M.sfree), kWorkers);
-        tc::mbar_init(tc::smem_u32(&M.kfull[0]), kWorkers);
-        tc::mbar_init(tc::smem_u32(&M.kfull[1]), kWorkers);
+        tc::mbar_init(tc::smem_u32(&M.kready), kWorkers);
         tc::mbar_init(tc::smem_u32(&M.pvfull), kWorkers);
         tc::mbar_init(tc::smem_u32(&M.mma2done), 1);
         tc::mbar_init(tc::smem_u32(&M.qready[0]), kWorkers);
@@ -501,9 +503,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
         tc::mbar_init(tc::smem_u32(&M.done), 1);
         for (int st = 0; st < kStages; ++st) {
             tc::mbar_init(tc::smem_u32(&M.rfull[st]), 1);
-            tc::mbar_init(tc::smem_u32(&M.rempty[st]), kWorkers);
+            tc::mbar_init(tc::smem_u32(&M.rempty[st]), 1);   // released by the MMA warp after pvfull
         }
         M.abort = 0;
+        for (int r = 0; r < kNR; ++r) M.nm[r] = 0.0f;   // a segment's first tile takes absolute logits
         tc::mbar_init_fence();
     }
     for (int e = tid; e < 64 * 32; e += kThreadsTc) {
@@ -527,104 +530,116 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
         const uint32_t lane_addr = tbase + ((uint32_t)(qd * 32) << 16);
         const uint32_t lut_lane = sm_u + kSmLut + (uint32_t)lane * 4u;
         const uint32_t rbar = kBarRed + g;
-        const int64_t seg0 = c0.seg;
+        const uint32_t b_sfull = tc::smem_u32(&M.sfull), b_kready = tc::smem_u32(&M.kready);
+        const uint32_t b_m2 = tc::smem_u32(&M.mma2done), b_pv = tc::smem_u32(&M.pvfull);
         // this thread's offsets inside a ring stage
-        const uint32_t key_off = kStKeys + (uint32_t)t * 128u;                  // + swizzled chunk
-        const uint32_t key_sw = (uint32_t)(t & 7);
+        const uint32_t key_a0 = kStKeys + (uint32_t)t * 128u + ((((uint32_t)(2 * g)) ^ (uint32_t)(t & 7)) << 4);
+        const uint32_t key_a1 = kStKeys + (uint32_t)t * 128u + ((((uint32_t)(2 * g + 1)) ^ (uint32_t)(t & 7)) << 4);
         const uint32_t val_off = kStVals + (uint32_t)(g * kD + t) * 12u;
         const uint32_t sc_off = kStScales + (uint32_t)t * 8u;
         const uint32_t nv_off = kStNorms + (uint32_t)t * 2u;
-        // key operand of tile j (ring stage j % kStages, already full) into TMEM key buffer j & 1
-        auto put_keys = [&](int j) {
-            const uint32_t st = sm_u + kSmRing + (uint32_t)(j % kStages) * kStageBytes + key_off;
-            uint4 kc[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t a = st + ((((uint32_t)(2 * g + h)) ^ key_sw) << 4);
-                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(kc[h].x), "=r"(kc[h].y), "=r"(kc[h].z), "=r"(kc[h].w)
-                             : "r"(a));
-            }
-            store_key_block(kc, lane_addr + kColK + (uint32_t)(j & 1) * 64u + 16u * g);
-            tc::wait_st();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.kfull[j & 1]));
-        };
-        auto wait_stage = [&](int j) {
-            tc::mbar_wait(tc::smem_u32(&M.rfull[j % kStages]), (uint32_t)((j / kStages) & 1), abortp, kTimeoutNs);
+        const uint32_t ring = sm_u + kSmRing;
+        // the last tile of a segment holds tokens [(nt - 1) * 128, n_ctx): this thread's token is valid there
+        // only if t < tail_lim
+        const int tail_lim = (int)(P.n_ctx - (int64_t)(nt - 1) * kTile);
+        auto seg_cursor = [&](int64_t seg, Cursor& c) {
+            c.seg = seg;
+            c.unit = seg / nrg;
+            c.rg = (int)(seg - c.unit * nrg);
+            c.ti = 0;
         };
 
-        // prologue: tile 0's key operand and the first segments' queries
-        Cursor c1 = c0, c2 = c0;
-        c1.adv(nt, nrg);
-        c2 = c1;
-        c2.adv(nt, nrg);
+        // prologue: the first segments' queries, then tile 0's key operand (-> kready phase 0)
+        int ti_c = c0.ti;                                   // tile index inside its segment: tiles i, i+1, i+2
+        int ti_1 = ti_c + 1 == nt ? 0 : ti_c + 1;
+        int ti_2 = ti_1 + 1 == nt ? 0 : ti_1 + 1;
+        int k_c = 0;                                        // segment ordinals (from this CTA's first) of i, i+1, i+2
+        int k_1 = ti_1 == 0 ? 1 : 0;
+        int k_2 = k_1 + (ti_2 == 0 ? 1 : 0);
         {
             uint4 qr[2];
             q_load(P, c0, g, qd, lane, qr);
             q_store<QBF16>(qr, sm_u + kSmQ, M, 0, g, qd, lane, P.scale_log2);
-            if (n > 1 && c1.ti == 0) {
+            if (n > 1 && ti_1 == 0) {
+                Cursor c1;
+                seg_cursor(c0.seg + 1, c1);
                 q_load(P, c1, g, qd, lane, qr);
                 q_store<QBF16>(qr, sm_u + kSmQ + 16384u, M, 1, g, qd, lane, P.scale_log2);
             }
-            wait_stage(0);
-            put_keys(0);
+            tc::mbar_wait(tc::smem_u32(&M.rfull[0]), 0u, abortp, kTimeoutNs);
+            uint4 kc[2];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[0].x), "=r"(kc[0].y), "=r"(kc[0].z), "=r"(kc[0].w) : "r"(ring + key_a0));
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[1].x), "=r"(kc[1].y), "=r"(kc[1].z), "=r"(kc[1].w) : "r"(ring + key_a1));
+            store_key_block(kc, lane_addr + kColK + 16u * g);
+            tc::wait_st();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(b_kready);
         }
 
-        Cursor cur = c0;
+        int st_c = 0, st_1 = kStages > 1 ? 1 : 0;          // ring stages of tiles i and i+1
+        uint32_t ph_1 = 0;                                  // phase of tile i+1's stage
         float2 l[8];
         float cst = 0.0f, wsc = 1.0f;
         int R = 0;
+        int64_t slot_c = 0;
         // a finished segment piece whose O is read out at the next tile (after its last MMA2)
         bool epi = false;
         int epi_R = 0;
         float epi_inv_w = 1.0f;
         int64_t epi_slot = 0;
         for (int i = 0; i < n; ++i) {
-            const bool first = (i == 0) || (cur.ti == 0);
-            const bool last = (i == n - 1) || (cur.ti == nt - 1);
+            const bool first = (i == 0) || (ti_c == 0);
+            const bool last = (i == n - 1) || (ti_c == nt - 1);
             if (first) {
-                R = min(kNR, P.Rtot - kNR * cur.rg);
-                cst = M.qc[(cur.seg - seg0) & 1][g];
-                wsc = unit_wscale(P.p.nmax[cur.unit]);
+                Cursor cs;
+                seg_cursor(c0.seg + k_c, cs);
+                R = min(kNR, P.Rtot - kNR * cs.rg);
+                cst = M.qc[k_c & 1][g];
+                wsc = unit_wscale(P.p.nmax[cs.unit]);
+                slot_c = cs.seg + cta;   // one partial per (segment, CTA): distinct
 #pragma unroll
                 for (int k = 0; k < 8; ++k) l[k] = make_float2(0.0f, 0.0f);
             }
-            const uint32_t stg = sm_u + kSmRing + (uint32_t)(i % kStages) * kStageBytes;
-            // -- a. key operand of tile i+1 (its buffer was last read by MMA1(i-1), complete), so that
-            //       MMA1(i+1) can start as soon as S(i) has been read; queries of tile i+2's segment
-            if (i + 1 < n) {
-                wait_stage(i + 1);
-                put_keys(i + 1);
-            }
-            const bool qprep = (i + 2 < n) && c2.ti == 0;
+            const uint32_t stg = ring + (uint32_t)st_c * kStageBytes;
+            const uint32_t stg1 = ring + (uint32_t)st_1 * kStageBytes;
+            // queries of tile i+2's segment, if it starts one (loaded now, stored at the end)
+            const bool qprep = (i + 2 < n) && ti_2 == 0;
             uint4 qr[2] = {};
-            if (qprep) q_load(P, c2, g, qd, lane, qr);
+            if (qprep) {
+                Cursor cq;
+                seg_cursor(c0.seg + k_2, cq);
+                q_load(P, cq, g, qd, lane, qr);
+            }
 
-            // -- b. S(i) = MMA1(i)
-            tc::mbar_wait(tc::smem_u32(&M.sfull), (uint32_t)(i & 1), abortp, kTimeoutNs);
+            // -- b. S(i) = MMA1(i); tile i+1's pool data (keys)
+            tc::mbar_wait(b_sfull, (uint32_t)(i & 1), abortp, kTimeoutNs);
             tc::fence_after();
+            const bool more = i + 1 < n;
+            if (more) tc::mbar_wait(tc::smem_u32(&M.rfull[st_1]), ph_1, abortp, kTimeoutNs);
 
-            // -- c. logits d = sum_b c_b S_b - m (absolute on a segment's first tile)
+            // -- c. logits d = sum_b c_b S_b - m (absolute on a segment's first tile: m = 0 then), with
+            //       tile i+1's key operand converted while the S loads are in flight
             uint2 scw;
             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(scw.x), "=r"(scw.y) : "r"(stg + sc_off));
-            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&scw.x));
-            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&scw.y));
-            const float cb0 = s01.x * cst, cb1 = s01.y * cst, cb2 = s23.x * cst, cb3 = s23.y * cst;
+            uint4 kc[2];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[0].x), "=r"(kc[0].y), "=r"(kc[0].z), "=r"(kc[0].w) : "r"(stg1 + key_a0));
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[1].x), "=r"(kc[1].y), "=r"(kc[1].z), "=r"(kc[1].w) : "r"(stg1 + key_a1));
             float2 d[8];
             {
-                // -m per row (the first tile of a segment takes absolute logits)
                 const float4* nmv = reinterpret_cast<const float4*>(&M.nm[kGRows * g]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float4 v = first ? make_float4(0.f, 0.f, 0.f, 0.f) : nmv[k];
+                    const float4 v = nmv[k];
                     d[2 * k] = make_float2(v.x, v.y);
                     d[2 * k + 1] = make_float2(v.z, v.w);
                 }
                 uint32_t sa[16], sb[16];
                 tc::tmem_ld16(lane_addr + kColS + 16u * g, sa);
                 tc::tmem_ld16(lane_addr + kColS + 64u + 16u * g, sb);
+                const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&scw.x));
+                const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&scw.y));
+                const float cb0 = s01.x * cst, cb1 = s01.y * cst, cb2 = s23.x * cst, cb3 = s23.y * cst;
                 tc::wait_ld();
                 const float2 c0x = make_float2(cb0, cb0), c1x = make_float2(cb1, cb1);
 #pragma unroll
@@ -634,11 +649,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
                 }
                 tc::tmem_ld16(lane_addr + kColS + 128u + 16u * g, sa);
                 tc::tmem_ld16(lane_addr + kColS + 192u + 16u * g, sb);
+                // tile i+1's key operand into the buffer MMA1(i-1) has finished reading
+                if (more) store_key_block(kc, lane_addr + kColK + (uint32_t)((i + 1) & 1) * 64u + 16u * g);
                 tc::wait_ld();
-                // S(i) has been read for the last time: MMA1(i+1) may overwrite it
+                tc::wait_st();
+                // S(i) has been read for the last time and the next key operand is in place: MMA1(i+1)
                 tc::fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.sfree));
+                if (lane == 0) tc::mbar_arrive(b_kready);
                 const float2 c2x = make_float2(cb2, cb2), c3x = make_float2(cb3, cb3);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -646,9 +664,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
                     d[k] = fma2(c3x, make_float2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1])), d[k]);
                 }
             }
-            const int64_t tok = (int64_t)cur.ti * kTile + t;
-            const bool valid = tok < P.n_ctx;
-            if ((int64_t)(cur.ti + 1) * kTile > P.n_ctx && !valid) {
+            const bool valid = ti_c != nt - 1 || t < tail_lim;
+            if (!valid) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) d[k] = make_float2(-INFINITY, -INFINITY);
             }
@@ -696,6 +713,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
             // -- d. probabilities: p = 2^d summed into l; P' = p * ||v|| * w in fp16
             uint32_t nvb;
             asm volatile("ld.shared.u16 %0, [%1];" : "=r"(nvb) : "r"(stg + nv_off));
+            uint32_t w0, w1, w2;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(stg + val_off));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(stg + val_off + 4u));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w2) : "r"(stg + val_off + 8u));
             const float nwf = valid ? __half2float(__ushort_as_half((unsigned short)nvb)) * wsc : 0.0f;
             const float2 nw2 = make_float2(nwf, nwf);
             uint32_t pk[8];
@@ -709,22 +730,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
             }
             // -- e. value operand of tile i: this coordinate's centroids for token quarter g
             uint32_t vv[16];
-            {
-                uint32_t w0, w1, w2;
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(stg + val_off));
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(stg + val_off + 4u));
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w2) : "r"(stg + val_off + 8u));
-                value_pairs(w0, w1, w2, lut_lane, vv);
-            }
-            // stage i has been read for the last time (its keys in the previous iteration): the TMA
-            // (an async-proxy write) may refill it
-            tc::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.rempty[i % kStages]));
+            value_pairs(w0, w1, w2, lut_lane, vv);
 
             // -- f. after MMA2(i-1): write out a finished piece's O, rescale O, publish V'(i), P'(i)
             if (i > 0) {
-                tc::mbar_wait(tc::smem_u32(&M.mma2done), (uint32_t)((i - 1) & 1), abortp, kTimeoutNs);
+                tc::mbar_wait(b_m2, (uint32_t)((i - 1) & 1), abortp, kTimeoutNs);
                 tc::fence_after();
             }
             if (epi) {
@@ -758,30 +768,40 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
             }
             tc::wait_st();
             tc::fence_before();
+            // orders this thread's reads of ring stage i (and P' writes) before the async proxy: the MMA
+            // warp releases the stage to the TMA once every worker has arrived here
             tc::fence_proxy_async();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.pvfull));
+            if (lane == 0) tc::mbar_arrive(b_pv);
             // -- g. end of a segment piece: its (m, l) now, its O after MMA2(i) (next tile or below)
             if (last) {
-                const int64_t slot = cur.seg + cta;   // one partial per (segment, CTA): distinct
-                write_row_stats(l, M, g, qd, lane, R, P.ws_ml + slot * P.RS * 2);
+                write_row_stats(l, M, g, qd, lane, R, P.ws_ml + slot_c * P.RS * 2);
                 epi = true;
                 epi_R = R;
                 epi_inv_w = 1.0f / wsc;
-                epi_slot = slot;
+                epi_slot = slot_c;
             }
             // -- h. queries of tile i+2's segment (its buffer was last used by the segment before
             //       tile i+1's, whose MMA1s have all completed)
-            if (qprep) {
-                const int qb = (int)((c2.seg - seg0) & 1);
-                q_store<QBF16>(qr, sm_u + kSmQ + (uint32_t)qb * 16384u, M, qb, g, qd, lane, P.scale_log2);
+            if (qprep)
+                q_store<QBF16>(qr, sm_u + kSmQ + (uint32_t)(k_2 & 1) * 16384u, M, k_2 & 1, g, qd, lane, P.scale_log2);
+            // advance the per-tile counters
+            st_c = st_1;
+            if (++st_1 == kStages) {
+                st_1 = 0;
+                ph_1 ^= 1u;
             }
-            cur = c1;
-            c1 = c2;
-            c2.adv(nt, nrg);
+            ti_c = ti_1;
+            ti_1 = ti_2;
+            k_c = k_1;
+            k_1 = k_2;
+            if (++ti_2 == nt) {
+                ti_2 = 0;
+                ++k_2;
+            }
         }
         if (epi) {
-            tc::mbar_wait(tc::smem_u32(&M.mma2done), (uint32_t)((n - 1) & 1), abortp, kTimeoutNs);
+            tc::mbar_wait(b_m2, (uint32_t)((n - 1) & 1), abortp, kTimeoutNs);
             tc::fence_after();
             uint32_t ov[16];
             tc::tmem_ld16(lane_addr + kColO + 16u * g, ov);
@@ -811,9 +831,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
                 if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&bar), ph, abortp, kTimeoutNs) ? 1 : 0;
                 return __shfl_sync(0xffffffffu, ok, 0) != 0;
             };
-            const int64_t seg0 = c0.seg;
             int ti = c0.ti;
-            int64_t seg = c0.seg;
+            int k = 0;                 // segment ordinal of tile i
+            int st_prev = 0;           // ring stage of tile i-1
             bool prev_first = true;
             int issued = 0;
             bool ok = P.test_stall == 0;
@@ -821,9 +841,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
                 bool cur_first = false;
                 if (i < n) {
                     cur_first = (i == 0) || (ti == 0);
-                    const int64_t k = seg - seg0;
-                    ok = wait0(M.kfull[i & 1], (uint32_t)((i >> 1) & 1));
-                    if (ok && i > 0) ok = wait0(M.sfree, (uint32_t)((i - 1) & 1));
+                    if (cur_first && i > 0) ++k;
+                    // tile i's key operand is in TMEM and S(i-1) has been read
+                    ok = wait0(M.kready, (uint32_t)(i & 1));
                     if (ok && cur_first) ok = wait0(M.qready[k & 1], (uint32_t)((k >> 1) & 1));
                     if (!ok) break;
                     tc::fence_after();
@@ -834,13 +854,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
                     ok = wait0(M.pvfull, (uint32_t)((i - 1) & 1));
                     if (!ok) break;
                     tc::fence_after();
+                    // every worker has read ring stage i-1 for the last time: the TMA may refill it
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&M.rempty[st_prev]));
                     issue_mma2(tO, tV, bp0 + (uint64_t)(((i - 1) & 1) * (16384 >> 4)), id2, prev_first ? 1u : 0u, b_m2);
                 }
                 __syncwarp();
                 prev_first = cur_first;
-                if (i < n && ++ti == nt) {
-                    ti = 0;
-                    ++seg;
+                if (i < n) {
+                    if (++ti == nt) ti = 0;
+                    st_prev = i % kStages;
                 }
             }
             if (P.test_stall) *abortp = 0;   // let the workers discover the stall on their own waits

@@ -140,16 +140,14 @@ __device__ __forceinline__ uint32_t bytes4(int a, int b, int c, int d) {
 }
 
 // One block of D threads per (unit, 32-token group) inside [t0, t0 + n). Phase 1: d/32 lanes per
-// token (token tau = lane group, quarter gl) do the keys and the value norm + FWHT as before and
-// leave the rotated coordinates y in shared memory. Phase 2: thread j = coordinate j takes the 32
-// tokens' y_j, decides their 3-bit codes and packs them into the coordinate's 12-byte string
-// (token k at bits 3k..3k+2). Tokens of a partly covered group that lie outside [t0, t0 + n) keep
+// token (token tau = lane group, quarter gl) do the keys, the value norm, FWHT and 3-bit decisions,
+// and leave the signed half-codes in shared memory. Phase 2: thread j = coordinate j packs the 32
+// tokens' codes of coordinate j into its 12-byte string (token k at bits 3k..3k+2). Tokens of a partly covered group that lie outside [t0, t0 + n) keep
 // the bits already in the pool.
 template <int D>
 struct EncSmem {
     static constexpr int kRow = D + 4;   // padded row of y (floats); chunks rotated, see enc_phys
-    float y[32][kRow];
-    float4 th[32];                       // per token: boundaries b4..b6 times ||v|| (+inf when ||v|| = 0)
+    float y[32][kRow];                   // per token: the signed half-codes of its coordinates
 };
 
 // physical float index of coordinate j inside a row of EncSmem::y: 16-byte chunk c of lane quarter gl
@@ -292,19 +290,23 @@ __global__ void __launch_bounds__(D, D == 128 ? 8 : 12) encode_kernel(const uint
             y[i + 1] = r.y;
         }
     }
-    // the rotated coordinates go to shared memory (rotated chunks, see enc_phys), with the token's
-    // norm-scaled boundaries; a zero norm gets infinite thresholds, so every code is 4 (u = 0)
+    // 3-bit decisions in registers: the signed half-code c - 3.5 of every coordinate, an exact float in
+    // {+-0.5, +-1.5, +-2.5, +-3.5}; a zero norm gives u = 0 and code 4; a token outside [t0, t0 + n)
+    // gets code 0 and keeps its old bits (phase 2)
+    {
+        const float t4 = __fmul_rn(kB4, nrm), t5 = __fmul_rn(kB5, nrm), t6 = __fmul_rn(kB6, nrm);
+        const float fill = nrm > 0.0f ? 0.0f : 0.5f;   // ||v|| = 0: every code is 4
+        const bool decide = valid && nrm > 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = decide ? value_half_code(y[i], t4, t5, t6) : (valid ? fill : -3.5f);
+    }
+    // the half-codes go to shared memory (rotated chunks, see enc_phys)
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         float4* dst = reinterpret_cast<float4*>(&sm.y[tau][enc_phys<D>(32 * gl + 4 * c)]);
         *dst = make_float4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
     }
-    if (gl == 0) {
-        const bool pos = nrm > 0.0f;
-        sm.th[tau] = pos ? make_float4(__fmul_rn(kB4, nrm), __fmul_rn(kB5, nrm), __fmul_rn(kB6, nrm), 0.0f)
-                         : make_float4(INFINITY, INFINITY, INFINITY, 0.0f);
-        if (valid) p.vn[pidx] = __float2half_rn(nrm);
-    }
+    if (gl == 0 && valid) p.vn[pidx] = __float2half_rn(nrm);
     // running per-unit maximum of ||v|| (an upper bound used by attention to scale fp16 operands):
     // one max-reduction per warp, one atomic per warp. Norms are non-negative, so their bit patterns
     // order as unsigned integers.
@@ -325,20 +327,13 @@ __global__ void __launch_bounds__(D, D == 128 ? 8 : 12) encode_kernel(const uint
         // eight codes c_0..c_7 -> the 24-bit group sum c_i * 8^i, formed exactly in fp32: Horner over
         // the half-codes h_i = c_i - 3.5 gives sum h_i 8^i, a multiple of 1/2 below 2^23 in magnitude
         // (24 significant bits at most, so every step is exact); adding 3.5 * sum 8^i = 8388607.5
-        // gives the integer group sum (< 2^24), also exactly. A token outside [t0, t0 + n) gets the
-        // half-code -3.5 (code 0) and its bits are taken from the pool below.
+        // gives the integer group sum (< 2^24), also exactly.
         uint32_t w24[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            float w = 0.0f;
+            float w = sm.y[8 * g + 7][pj];
 #pragma unroll
-            for (int i = 7; i >= 0; --i) {
-                const int kk = 8 * g + i;
-                const float4 th = sm.th[kk];
-                float h = value_half_code(sm.y[kk][pj], th.x, th.y, th.z);
-                if (kk < kmin || kk >= kmax) h = -3.5f;
-                w = (i == 7) ? h : fmaf(w, 8.0f, h);
-            }
+            for (int i = 6; i >= 0; --i) w = fmaf(w, 8.0f, sm.y[8 * g + i][pj]);
             w24[g] = (uint32_t)__float2uint_rz(w + 8388607.5f);
         }
         uint32_t o0 = w24[0] | (w24[1] << 24);
