@@ -287,6 +287,50 @@ __device__ __forceinline__ int64_t merge_range_of(int64_t x, int nc, int64_t tt)
     return num / tt;
 }
 
+// Finishes one output row from its merged rotated-basis accumulator o (this lane's D/32 elements),
+// running maximum M and sum L: the inverse FWHT (1/D) H o, then the private suffix's partial (already
+// in the original basis) under the same softmax, then the division by the total sum.
+template <int D>
+__device__ __forceinline__ void finish_row(float (&o)[D / 32], float M, float L, float2 sml,
+                                           const typename MergeVec<D>::T& sv, int lane) {
+    constexpr int EPL = D / 32;
+    using V = MergeVec<D>;
+    // in-lane butterflies (strides < EPL), then across lanes
+#pragma unroll
+    for (int h = 1; h < EPL; h <<= 1)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+            if ((e & h) == 0) {
+                const float x = o[e], y = o[e + h];
+                o[e] = x + y;
+                o[e + h] = x - y;
+            }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const float other = __shfl_xor_sync(0xffffffffu, o[e], m);
+            o[e] = upper ? other - o[e] : o[e] + other;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] *= (1.0f / D);
+    if (sml.x != -INFINITY) {
+        // the suffix partial is already in the original basis
+        const float Mn = fmaxf(M, sml.x);
+        const float c = exp2f(M - Mn), w = exp2f(sml.x - Mn);
+        float x[EPL];
+        V::to(sv, x);
+        L = fmaf(w, sml.y, L * c);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, x[e], o[e] * c);
+    }
+    const float inv = 1.0f / L;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] *= inv;
+}
+
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) attend_merge(const float* __restrict__ ws_acc,
                                                                  const float* __restrict__ ws_ml,
@@ -298,6 +342,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps) attend_merge(const float* __
     using V = MergeVec<D>;
     const int64_t wid = (int64_t)blockIdx.x * kMergeWarps + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    // launched as a programmatic dependent of the partial kernel: wait until its writes are visible
+    // (a no-op for an ordinary launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (wid >= (int64_t)U * R) return;
     const int unit = (int)(wid / R), r = (int)(wid % R);
     const int G = Hq / H;
@@ -361,41 +408,100 @@ __global__ void __launch_bounds__(32 * kMergeWarps) attend_merge(const float* __
         }
         M = Mn;
     }
-    // in-lane butterflies (strides < EPL), then across lanes
+    finish_row<D>(o, M, L, sml, sv, lane);
+    reinterpret_cast<typename V::T*>(out + orow * D)[lane] = V::from(o);
+}
+
+// Merge for the tensor-core partition: blockIdx.x is a segment (kv-head unit x row group of up to 64
+// rows), blockIdx.y a block of 32 of its rows, four rows per warp. The segment's pieces are the slots
+// s + c for the CTAs c whose contiguous tile ranges overlap the segment (at most two for segments
+// longer than a CTA's range, the usual case). Index arithmetic is done once per block, and a warp
+// issues the loads of all its rows' first two pieces (and suffix partials) before using any, so the
+// whole merge costs about one memory round trip per warp.
+constexpr int kMergeRowsPerWarp = 4;
+template <int D>
+__global__ void __launch_bounds__(32 * kMergeWarps) attend_merge_tc(const float* __restrict__ ws_acc,
+                                                                    const float* __restrict__ ws_ml,
+                                                                    float* __restrict__ out, int H, int A, int Hq,
+                                                                    int Rtot, MergeLayout lay,
+                                                                    const float* __restrict__ sfx_acc,
+                                                                    const float* __restrict__ sfx_ml) {
+    constexpr int EPL = D / 32;
+    constexpr int RW = kMergeRowsPerWarp;
+    using V = MergeVec<D>;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int s = blockIdx.x;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int unit = s / lay.nrg, rg = s - unit * lay.nrg;
+    const int layer = unit / H, kvh = unit - layer * H;
+    const int G = Hq / H;
+    const int rows = min(lay.RS, Rtot - rg * lay.RS);
+    const int64_t x0 = (int64_t)s * lay.nt;                      // the segment's first tile
+    const int lo = (int)(((x0 + 1) * lay.nc - 1) / lay.tt);      // CTA holding its first tile
+    const int hi = (int)(((x0 + lay.nt) * lay.nc - 1) / lay.tt); // CTA holding its last tile
+    const int pieces = hi - lo + 1;
+    const int rbase = blockIdx.y * (kMergeWarps * RW) + warp * RW;
+
+    float2 ml[RW][2], sml[RW];
+    typename V::T v[RW][2], sv[RW];
+    int64_t orow[RW];
 #pragma unroll
-    for (int h = 1; h < EPL; h <<= 1)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e)
-            if ((e & h) == 0) {
-                const float x = o[e], y = o[e + h];
-                o[e] = x + y;
-                o[e + h] = x - y;
+    for (int k = 0; k < RW; ++k) {
+        const int r = rbase + k;
+        orow[k] = 0;
+        sml[k] = make_float2(-INFINITY, 0.0f);
+        ml[k][0] = ml[k][1] = make_float2(-INFINITY, 0.0f);
+        if (r < rows) {
+            const int R0 = rg * lay.RS + r;
+            const int a = R0 / G, g = R0 - a * G;
+            orow[k] = ((int64_t)layer * A + a) * Hq + kvh * G + g;
+            if (sfx_ml) {
+                sml[k] = reinterpret_cast<const float2*>(sfx_ml)[orow[k]];
+                sv[k] = reinterpret_cast<const typename V::T*>(sfx_acc + orow[k] * D)[lane];
             }
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const float other = __shfl_xor_sync(0xffffffffu, o[e], m);
-            o[e] = upper ? other - o[e] : o[e] + other;
+            for (int i = 0; i < 2; ++i)
+                if (i < pieces) {
+                    const int64_t pr = (int64_t)(s + lo + i) * lay.RS + r;
+                    ml[k][i] = reinterpret_cast<const float2*>(ws_ml)[pr];
+                    v[k][i] = reinterpret_cast<const typename V::T*>(ws_acc + pr * D)[lane];
+                }
         }
     }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] *= (1.0f / D);
-    if (sml.x != -INFINITY) {
-        // the suffix partial is already in the original basis
-        const float Mn = fmaxf(M, sml.x);
-        const float c = exp2f(M - Mn), w = exp2f(sml.x - Mn);
-        float x[EPL];
-        V::to(sv, x);
-        L = fmaf(w, sml.y, L * c);
+    for (int k = 0; k < RW; ++k) {
+        const int r = rbase + k;
+        if (r >= rows) continue;
+        float M = fmaxf(ml[k][0].x, ml[k][1].x), L = 0.0f;
+        float o[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, x[e], o[e] * c);
+        for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (ml[k][i].x == -INFINITY) continue;
+            const float w = exp2f(ml[k][i].x - M);
+            L = fmaf(w, ml[k][i].y, L);
+            float x[EPL];
+            V::to(v[k][i], x);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, x[e], o[e]);
+        }
+        for (int i = 2; i < pieces; ++i) {   // segments split over more than two CTAs
+            const int64_t pr = (int64_t)(s + lo + i) * lay.RS + r;
+            const float2 mi = reinterpret_cast<const float2*>(ws_ml)[pr];
+            if (mi.x == -INFINITY) continue;
+            float x[EPL];
+            V::to(reinterpret_cast<const typename V::T*>(ws_acc + pr * D)[lane], x);
+            const float Mn = fmaxf(M, mi.x);
+            const float c = exp2f(M - Mn), w = exp2f(mi.x - Mn);
+            L = fmaf(w, mi.y, L * c);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, x[e], o[e] * c);
+            M = Mn;
+        }
+        finish_row<D>(o, M, L, sml[k], sv[k], lane);
+        reinterpret_cast<typename V::T*>(out + orow[k] * D)[lane] = V::from(o);
     }
-    const float inv = 1.0f / L;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] *= inv;
-    reinterpret_cast<typename V::T*>(out + orow * D)[lane] = V::from(o);
 }
 
 template <int D, int RMAX, bool BF16>
@@ -450,11 +556,31 @@ polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float
                                   const float* sfx_acc, const float* sfx_ml) {
     const int64_t warps = (int64_t)U * R;
     const unsigned blocks = (unsigned)((warps + kMergeWarps - 1) / kMergeWarps);
-    if (D == 128)
-        attend_merge<128><<<blocks, 32 * kMergeWarps, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
-    else
-        attend_merge<64><<<blocks, 32 * kMergeWarps, 0, st>>>(ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay, sfx_acc, sfx_ml);
-    const cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the merge's CTAs may be scheduled while the partial kernel's last
+    // CTAs finish; each waits (griddepcontrol.wait) for the partials before reading them
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(32 * kMergeWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (lay.nc > 0) {
+        constexpr int rows_per_block = kMergeWarps * kMergeRowsPerWarp;
+        cfg.gridDim = dim3((unsigned)((int64_t)U * lay.nrg), (unsigned)((lay.RS + rows_per_block - 1) / rows_per_block));
+        e = D == 128 ? cudaLaunchKernelEx(&cfg, attend_merge_tc<128>, ws_acc, ws_ml, out, H, A, Hq, R, lay, sfx_acc, sfx_ml)
+                     : cudaLaunchKernelEx(&cfg, attend_merge_tc<64>, ws_acc, ws_ml, out, H, A, Hq, R, lay, sfx_acc, sfx_ml);
+    } else {
+        e = D == 128 ? cudaLaunchKernelEx(&cfg, attend_merge<128>, ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay,
+                                          sfx_acc, sfx_ml)
+                     : cudaLaunchKernelEx(&cfg, attend_merge<64>, ws_acc, ws_ml, out, U, H, A, Hq, R, n_slots, lay,
+                                          sfx_acc, sfx_ml);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend merge launch: %s", cudaGetErrorString(e));
     return POLYKV_OK;
 }

@@ -206,9 +206,11 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool pred) {
 __device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_shared32(uint32_t addr) {
+// load from the centroid-pair table, which is read-only after set-up: not volatile, so the compiler
+// may schedule it freely
+__device__ __forceinline__ uint32_t ld_table32(uint32_t addr) {
     uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
 
@@ -258,7 +260,7 @@ __device__ __forceinline__ uint32_t pair_off(uint32_t w0, uint32_t w1, uint32_t 
 // The 32 value codes of one coordinate (one 12-byte string) -> 16 fp16 centroid pairs.
 __device__ __forceinline__ void value_pairs(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t lut_lane,
                                             uint32_t (&o)[16]) {
-#define PKV_PAIR(C) o[C] = ld_shared32(lut_lane | pair_off<C>(w0, w1, w2));
+#define PKV_PAIR(C) o[C] = ld_table32(lut_lane | pair_off<C>(w0, w1, w2));
     PKV_PAIR(0) PKV_PAIR(1) PKV_PAIR(2) PKV_PAIR(3) PKV_PAIR(4) PKV_PAIR(5) PKV_PAIR(6) PKV_PAIR(7)
     PKV_PAIR(8) PKV_PAIR(9) PKV_PAIR(10) PKV_PAIR(11) PKV_PAIR(12) PKV_PAIR(13) PKV_PAIR(14) PKV_PAIR(15)
 #undef PKV_PAIR
@@ -516,6 +518,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
         lut[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
     }
     if (warp == kWarpMma) tc::tmem_alloc(tc::smem_u32(&M.tslot), kTmemCols);
+    // the merge kernel (a programmatic dependent) may be scheduled as this grid's CTAs retire; it waits
+    // for this grid's completion before it reads the partials
+    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -538,7 +543,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
         const uint32_t val_off = kStVals + (uint32_t)(g * kD + t) * 12u;
         const uint32_t sc_off = kStScales + (uint32_t)t * 8u;
         const uint32_t nv_off = kStNorms + (uint32_t)t * 2u;
-        const uint32_t ring = sm_u + kSmRing;
         // the last tile of a segment holds tokens [(nt - 1) * 128, n_ctx): this thread's token is valid there
         // only if t < tail_lim
         const int tail_lim = (int)(P.n_ctx - (int64_t)(nt - 1) * kTile);
@@ -568,8 +572,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
             }
             tc::mbar_wait(tc::smem_u32(&M.rfull[0]), 0u, abortp, kTimeoutNs);
             uint4 kc[2];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[0].x), "=r"(kc[0].y), "=r"(kc[0].z), "=r"(kc[0].w) : "r"(ring + key_a0));
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[1].x), "=r"(kc[1].y), "=r"(kc[1].z), "=r"(kc[1].w) : "r"(ring + key_a1));
+            kc[0] = *reinterpret_cast<const uint4*>(sm + kSmRing + key_a0);
+            kc[1] = *reinterpret_cast<const uint4*>(sm + kSmRing + key_a1);
             store_key_block(kc, lane_addr + kColK + 16u * g);
             tc::wait_st();
             tc::fence_before();
@@ -601,8 +605,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
 #pragma unroll
                 for (int k = 0; k < 8; ++k) l[k] = make_float2(0.0f, 0.0f);
             }
-            const uint32_t stg = ring + (uint32_t)st_c * kStageBytes;
-            const uint32_t stg1 = ring + (uint32_t)st_1 * kStageBytes;
+            const uint8_t* stgp = sm + kSmRing + (uint32_t)st_c * kStageBytes;
+            const uint8_t* stgp1 = sm + kSmRing + (uint32_t)st_1 * kStageBytes;
             // queries of tile i+2's segment, if it starts one (loaded now, stored at the end)
             const bool qprep = (i + 2 < n) && ti_2 == 0;
             uint4 qr[2] = {};
@@ -620,11 +624,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
 
             // -- c. logits d = sum_b c_b S_b - m (absolute on a segment's first tile: m = 0 then), with
             //       tile i+1's key operand converted while the S loads are in flight
-            uint2 scw;
-            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(scw.x), "=r"(scw.y) : "r"(stg + sc_off));
+            const uint2 scw = *reinterpret_cast<const uint2*>(stgp + sc_off);
             uint4 kc[2];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[0].x), "=r"(kc[0].y), "=r"(kc[0].z), "=r"(kc[0].w) : "r"(stg1 + key_a0));
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(kc[1].x), "=r"(kc[1].y), "=r"(kc[1].z), "=r"(kc[1].w) : "r"(stg1 + key_a1));
+            kc[0] = *reinterpret_cast<const uint4*>(stgp1 + key_a0);
+            kc[1] = *reinterpret_cast<const uint4*>(stgp1 + key_a1);
             float2 d[8];
             {
                 const float4* nmv = reinterpret_cast<const float4*>(&M.nm[kGRows * g]);
@@ -711,12 +714,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
                 resc = !first;
             }
             // -- d. probabilities: p = 2^d summed into l; P' = p * ||v|| * w in fp16
-            uint32_t nvb;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(nvb) : "r"(stg + nv_off));
-            uint32_t w0, w1, w2;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(stg + val_off));
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(stg + val_off + 4u));
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w2) : "r"(stg + val_off + 8u));
+            const uint32_t nvb = *reinterpret_cast<const unsigned short*>(stgp + nv_off);
+            const uint32_t* vsrc = reinterpret_cast<const uint32_t*>(stgp + val_off);
+            const uint32_t w0 = vsrc[0], w1 = vsrc[1], w2 = vsrc[2];
             const float nwf = valid ? __half2float(__ushort_as_half((unsigned short)nvb)) * wsc : 0.0f;
             const float2 nw2 = make_float2(nwf, nwf);
             uint32_t pk[8];
