@@ -201,9 +201,12 @@ POLYKV_API polykv_status polykv_attend_ex(const polykv_pool* pool, const void* q
  * library's device module (held on every GPU that loads the library until the process exits).
  * Arguments and output are those of polykv_attend; nothing is allocated. Arguments that would
  * need more than 16 MiB of partials return POLYKV_E_BUFFER_TOO_SMALL with a message (the
- * Llama-3-8B shape with 15 agents needs about 16.0 MB on a 152-SM GB300).
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
- * caches it; make that first call before any stream capture. All calls share the one array:
+ * Llama-3-8B shape with 15 agents needs about 12.7 MB on a 152-SM GB300, at any context length:
+ * the partials grow with the SM count and the number of kv-head units, not with n_ctx).
+ * The first call in a CUDA context looks up the array's device address (cudaGetSymbolAddress)
+ * and caches it with the context's unique id; a call in another context looks it up again. The
+ * cached address does not survive cudaDeviceReset: the next call (in the new primary context)
+ * makes a fresh lookup. Make the first call in a context before any stream capture. All calls share the one array:
  * calls that may overlap on the GPU (other streams, other host threads) race on it and must be
  * ordered by the caller. The array keeps the last call's partials; every call writes each slot it
  * reads, so nothing needs clearing between calls. */

@@ -9,6 +9,9 @@
 #include <mutex>
 #include <new>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "polykv_internal.cuh"
 
 struct polykv_pool {
@@ -205,30 +208,72 @@ polykv_status polykv_attend(const polykv_pool* pool, const void* q, float* out, 
 // file-scope device array instead. The array is part of the library's module, so every GPU that
 // loads the library holds it until the process exits; its size is therefore kept modest and
 // fixed: 16 MiB, enough for the Llama-3-8B shape (32 layers x 8 kv heads, 15 agents x 4 query
-// heads, any context length on a 152-SM GB300).
+// heads, any context length on a 152-SM GB300: about 12.7 MB).
 namespace polykv {
 constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
 static __device__ __align__(256) unsigned char g_attend_scratch[kStaticScratchBytes];
-static void* g_scratch_dev_ptr[128] = {nullptr};
+struct ScratchAddr {
+    unsigned long long ctx_id;   // unique id of the context the address was looked up in (0: none)
+    void* ptr;
+};
+static ScratchAddr g_scratch_addr[128] = {};
 static std::mutex g_scratch_mu;
 
-// Device address of the scratch array for the current device. Host code only sees a host-side
-// stand-in for the symbol, so the address is looked up once per device (the first call on a
-// device) and cached.
+// Unique id of the calling thread's current CUDA context (0 if none), via cuCtxGetCurrent and
+// cuCtxGetId from the driver, looked up once (no link-time dependency on libcuda). Ids, unlike
+// context handles, are never reused within a process.
+static polykv_status current_ctx_id(unsigned long long* id) {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_cur || !get_id) return set_error(POLYKV_E_CUDA, "attend_static: cuCtxGetCurrent/cuCtxGetId not available");
+    CUcontext ctx = nullptr;
+    if (get_cur(&ctx) != CUDA_SUCCESS) return set_error(POLYKV_E_CUDA, "attend_static: cuCtxGetCurrent failed");
+    *id = 0;
+    if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return set_error(POLYKV_E_CUDA, "attend_static: cuCtxGetId failed");
+    return POLYKV_OK;
+}
+
+// Device address of the scratch array in the current device's current context. Host code only
+// sees a host-side stand-in for the symbol, so the address is looked up on the first call in a
+// context and cached with that context's id. A call made in another context (the primary context
+// re-created after cudaDeviceReset, or a context the caller made current) looks it up again: the
+// module, and so the array, is loaded anew in every context.
 static polykv_status static_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_static: cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 128) return set_error(POLYKV_E_UNSUPPORTED, "attend_static: device %d", dev);
+    unsigned long long id = 0;
+    polykv_status st = current_ctx_id(&id);
+    if (st != POLYKV_OK) return st;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_dev_ptr[dev]) {
+    ScratchAddr& a = g_scratch_addr[dev];
+    if (id == 0 || !a.ptr || a.ctx_id != id) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_attend_scratch);
+        e = cudaGetSymbolAddress(&p, g_attend_scratch);   // makes the primary context current if none is
         if (e != cudaSuccess || !p)
             return set_error(POLYKV_E_CUDA, "attend_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        g_scratch_dev_ptr[dev] = p;
+        if (id == 0) {
+            st = current_ctx_id(&id);
+            if (st != POLYKV_OK) return st;
+            if (id == 0) return set_error(POLYKV_E_CUDA, "attend_static: no current CUDA context");
+        }
+        a.ctx_id = id;
+        a.ptr = p;
     }
-    *out = g_scratch_dev_ptr[dev];
+    *out = a.ptr;
     return POLYKV_OK;
 }
 }  // namespace polykv
