@@ -204,26 +204,78 @@ def run_reference(args, w: synth.Workload):
     return 0
 
 
-def cpu_baseline(w: synth.Workload):
-    """Oracle timed on a bounded sample (1 layer) of the workload, scaled to GB/s."""
+def _oracle_layer(job):
+    """One layer of the workload through the CPU oracle, encode and attend timed separately. Runs in a
+    spawned worker process with one BLAS thread (set by _one_thread before numpy is imported)."""
+    name, layer_seed, n_layers_override = job
     import oracle
+    w = synth.WORKLOADS[name]
     c32, b32 = oracle.codebook.codebook_f32()
-    kb, vb = synth.gen_kv(1, w.n_kv_heads, w.n_ctx, w.head_dim, w.dtype, 0)
-    qb = synth.gen_q(1, w.n_agents, w.n_q_heads, w.head_dim, w.dtype, 0)
-    enc_b, att_b = algorithmic_bytes(w, w.n_ctx, w.n_agents)
+    kb, vb = synth.gen_kv(1, w.n_kv_heads, w.n_ctx, w.head_dim, w.dtype, layer_seed)
+    qb = synth.gen_q(1, w.n_agents, w.n_q_heads, w.head_dim, w.dtype, layer_seed)
     t0 = time.perf_counter()
-    reps = 0
-    while True:
-        pool = oracle.attention.encode_pool(kb, vb, w.dtype, b32)
-        oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32)
-        reps += 1
-        if time.perf_counter() - t0 > 10.0 or reps >= 20:
-            break
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": (enc_b + att_b) / w.n_layers / dt / 1e9, "unit": "GB/s",
-            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{reps} x (encode + attend of 1 of {w.n_layers} layers, all heads/agents); numpy, "
-                      f"BLAS threads up to the core count"}
+    pool = oracle.attention.encode_pool(kb, vb, w.dtype, b32)
+    t1 = time.perf_counter()
+    oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+class _one_thread_env:
+    """Sets the BLAS/OpenMP thread counts to 1 while worker processes are spawned: a spawned child reads
+    them when it first imports numpy, which happens before any pool initializer runs."""
+    names = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+    def __enter__(self):
+        self.old = {v: os.environ.get(v) for v in self.names}
+        os.environ.update({v: "1" for v in self.names})
+
+    def __exit__(self, *exc):
+        for v, old in self.old.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+
+
+def cpu_baseline(w: synth.Workload, budget_s: float = 20.0):
+    """The CPU oracle, as it stands, on a bounded sample of the workload (whole layers), in two variants:
+    one process with one thread, and one single-threaded process per host core working on different
+    layers at once. Encode and attend are timed separately; throughputs are scaled to the full workload's
+    algorithmic bytes (GB/s) and tokens/s. Processes are spawned, so this is safe after GPU work."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    enc_b, att_b = algorithmic_bytes(w, w.n_ctx, w.n_agents)
+    enc_l, att_l = enc_b / w.n_layers, att_b / w.n_layers          # bytes per layer
+    ctx = mp.get_context("spawn")
+    t_start = time.perf_counter()
+    with _one_thread_env(), ctx.Pool(processes=1) as pool:
+        single = pool.map(_oracle_layer, [(w.name, 0, None)])
+    se, sa = single[0]
+    # all cores: as many one-layer jobs as fit in the budget, one per core per round
+    rounds = max(1, min(4, int(budget_s / max(se + sa, 1e-3) / 2)))
+    with _one_thread_env(), ctx.Pool(processes=cores) as pool:
+        pool.map(abs, range(cores))                                    # workers up before the clock starts
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_layer, [(w.name, 100 + i, None) for i in range(cores * rounds)], chunksize=1)
+        wall = time.perf_counter() - t0
+    enc_sum = sum(r[0] for r in res)
+    att_sum = sum(r[1] for r in res)
+    n_lay = len(res)
+    # the all-core wall time covers encode + attend of n_lay layers; split it in proportion to CPU time
+    enc_wall = wall * enc_sum / (enc_sum + att_sum)
+    att_wall = wall - enc_wall
+    all_gbs = n_lay * (enc_l + att_l) / wall / 1e9
+    return {"value": all_gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_lay} layers of {w.n_layers} (encode + attend, all kv heads and agents), one "
+                      f"single-threaded spawned process per core; single-thread variant: 1 layer",
+            "all_cores": {"gbs": all_gbs, "encode_tokens_per_s": n_lay * w.n_ctx / w.n_layers / enc_wall,
+                          "encode_gbs": n_lay * enc_l / enc_wall / 1e9,
+                          "attend_gbs": n_lay * att_l / att_wall / 1e9, "processes": cores, "layers": n_lay},
+            "single_thread": {"gbs": (enc_l + att_l) / (se + sa) / 1e9,
+                              "encode_tokens_per_s": w.n_ctx / w.n_layers / se, "encode_gbs": enc_l / se / 1e9,
+                              "attend_gbs": att_l / sa / 1e9, "encode_s_per_layer": se, "attend_s_per_layer": sa},
+            "seconds": time.perf_counter() - t_start}
 
 
 # ----------------------------------------------------------------------------- polykv arm
@@ -295,8 +347,8 @@ def run_polykv(args, w: synth.Workload):
     clocks = sampler.stop()
     enc_ms = [e[0].elapsed_time(e[1]) for e in ev]
     att_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    step_ms = float(np.mean([a + b for a, b in zip(enc_ms, att_ms)]))
-    enc_ms_m, att_ms_m = float(np.mean(enc_ms)), float(np.mean(att_ms))
+    step_ms = float(np.mean([a + b for a, b in zip(enc_ms, att_ms)]))        # the K timed steps' average
+    enc_ms_m, att_ms_m = float(np.median(enc_ms)), float(np.median(att_ms))  # per-kernel medians
 
     # attention alone, L2 flushed before each launch (the pool is read from HBM)
     att_alone = []
@@ -308,7 +360,7 @@ def run_polykv(args, w: synth.Workload):
         e1.record(stream)
         e1.synchronize()
         att_alone.append(e0.elapsed_time(e1))
-    att_alone_ms = float(np.mean(att_alone))
+    att_alone_ms = float(np.median(att_alone))
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     hk = torch.from_numpy(kb.view(np.int16)).pin_memory()
@@ -328,7 +380,7 @@ def run_polykv(args, w: synth.Workload):
         torch.cuda.synchronize()
         if i > 0:
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e_ms_m = float(np.mean(e2e_ms)) if e2e_ms else float("nan")
+    e2e_ms_m = float(np.median(e2e_ms)) if e2e_ms else float("nan")
 
     def allmax(x):
         return max_over_ranks(x, world, dev)
@@ -456,8 +508,9 @@ def run_sweep(args):
                               max(2, args.steps // 4))
                 R = A * C * (Hq // H)
                 flops = 4.0 * R * T * d * L * H + 4.0 * (C * (C + 1) / 2) * (Hq // H) * d * L * A * H
-                # tensor-core MMAs issued: keys twice (exact hi/lo halves), values once; rows padded to 64
-                mma_flops = 2.0 * 128 * 64 * 16 * (16 + 8) * ((R + 63) // 64) * ((T + 127) // 128) * L * H
+                # tensor-core MMAs issued (M=128, N=64, K=16): 8 for the keys (4 q8_0 blocks x 2 K-steps)
+                # and 8 for the values per 128-token tile and row group of up to 64 query rows
+                mma_flops = 2.0 * 128 * 64 * 16 * (8 + 8) * ((R + 63) // 64) * ((T + 127) // 128) * L * H
                 rows.append({"mode": "attend_chunk", "n_ctx": T, "n_agents": A, "chunk": C, "us": ch_us,
                              "query_tokens_per_s": A * C / (ch_us * 1e-6),
                              "tflops": flops / (ch_us * 1e-6) / 1e12,
@@ -476,7 +529,7 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="polykv", choices=["polykv", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
