@@ -68,19 +68,45 @@ static polykv_status compute_regions(const polykv_pool_desc* d, polykv_pool_regi
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Which attention kernel serves a call: the tensor-core path for head_dim 128
-// and up to 64 rows per kv head, the CUDA-core path otherwise. The
-// environment variable POLYKV_ATTEND_PATH=simt|tc overrides (tc only where
-// supported) so both paths can be checked on the same shapes.
-static bool use_tc_path(const PoolView& p, int rows) {
+// Which attention kernel serves a call: the warp-level kernel when a kv head
+// has few query rows (head_dim 64 with up to 8, 128 with up to 4), the
+// tensor-core kernel for head_dim 128 and more rows, the CUDA-core kernel
+// otherwise. The environment variable POLYKV_ATTEND_PATH=simt|tc|warp
+// overrides (tc and warp only where supported) so the paths can be checked
+// against each other on the same shapes.
+enum class AttendPath { Simt, Tc, Warp };
+
+static AttendPath attend_path(const PoolView& p, int rows) {
     const bool tc_ok = attend_tc_supported(p, rows);
+    const bool warp_ok = attend_warp_supported(p, rows);
     const char* e = getenv("POLYKV_ATTEND_PATH");
-    if (e && strcmp(e, "simt") == 0) return false;
-    return tc_ok;
+    if (e && strcmp(e, "simt") == 0) return AttendPath::Simt;
+    if (e && strcmp(e, "tc") == 0 && tc_ok) return AttendPath::Tc;
+    if (e && strcmp(e, "warp") == 0 && warp_ok) return AttendPath::Warp;
+    if (warp_ok) return AttendPath::Warp;
+    return tc_ok ? AttendPath::Tc : AttendPath::Simt;
 }
 
 static size_t attend_workspace(const PoolView& p, int rows, int64_t n_ctx) {
-    return use_tc_path(p, rows) ? attend_tc_workspace(p, rows, n_ctx) : attend_simt_workspace(p, rows, n_ctx);
+    switch (attend_path(p, rows)) {
+        case AttendPath::Warp: return attend_warp_workspace(p, rows, n_ctx);
+        case AttendPath::Tc: return attend_tc_workspace(p, rows, n_ctx);
+        default: return attend_simt_workspace(p, rows, n_ctx);
+    }
+}
+
+static polykv_status launch_pool_attend(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
+                                        int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
+                                        cudaStream_t st, const SuffixArgs* sfx = nullptr) {
+    const int rows = n_agents * (n_q_heads / p.H);
+    switch (attend_path(p, rows)) {
+        case AttendPath::Warp:
+            return launch_attend_warp(p, dt, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, st, sfx);
+        case AttendPath::Tc:
+            return launch_attend_tc(p, dt, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, st, sfx);
+        default:
+            return launch_attend_simt(p, dt, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, st, sfx);
+    }
 }
 
 }  // namespace polykv
@@ -192,10 +218,7 @@ polykv_status polykv_attend(const polykv_pool* pool, const void* q, float* out, 
     const size_t need = attend_workspace(pool->view, rows, n_ctx);
     if (need > 0 && !workspace) return set_error(POLYKV_E_INVAL, "workspace is NULL but %zu bytes are needed", need);
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
-    if (use_tc_path(pool->view, rows))
-        return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
-                                workspace_bytes, static_cast<cudaStream_t>(stream));
-    return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
+    return launch_pool_attend(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
                               workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -295,10 +318,7 @@ polykv_status polykv_attend_static_ws(const polykv_pool* pool, const void* q, fl
     const polykv_status s2 = static_scratch(&ws);
     if (s2 != POLYKV_OK) return s2;
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
-    if (use_tc_path(pool->view, rows))
-        return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, ws,
-                                kStaticScratchBytes, static_cast<cudaStream_t>(stream));
-    return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, ws,
+    return launch_pool_attend(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, ws,
                               kStaticScratchBytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -387,10 +407,7 @@ polykv_status polykv_attend_ex(const polykv_pool* pool, const void* q, float* ou
         chk.acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(pool_ws));
         chk.ml = chk.acc + nrows * (size_t)pool->desc.head_dim;
         const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
-        if (use_tc_path(pool->view, rows))
-            return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, (int)av, n_q_heads, n_ctx, scale,
-                                    workspace, pool_ws, static_cast<cudaStream_t>(stream), &chk);
-        return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, (int)av, n_q_heads, n_ctx, scale,
+        return launch_pool_attend(pool->view, pool->desc.in_dtype, q, out, (int)av, n_q_heads, n_ctx, scale,
                                   workspace, pool_ws, static_cast<cudaStream_t>(stream), &chk);
     }
     if (!q || !out || !workspace) return set_error(POLYKV_E_INVAL, "q, out and workspace must be non-NULL");
@@ -415,10 +432,7 @@ polykv_status polykv_attend_ex(const polykv_pool* pool, const void* q, float* ou
     sfx.acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(pool_ws));
     sfx.ml = sfx.acc + nrows * (size_t)pool->desc.head_dim;
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)pool->desc.head_dim);
-    if (use_tc_path(pool->view, rows))
-        return launch_attend_tc(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
-                                pool_ws, static_cast<cudaStream_t>(stream), &sfx);
-    return launch_attend_simt(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
+    return launch_pool_attend(pool->view, pool->desc.in_dtype, q, out, n_agents, n_q_heads, n_ctx, scale, workspace,
                               pool_ws, static_cast<cudaStream_t>(stream), &sfx);
 }
 

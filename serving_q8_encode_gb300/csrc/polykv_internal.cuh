@@ -28,7 +28,7 @@ constexpr float kB6 = (kC6 + kC7) * 0.5f;
 struct PoolView {
     int8_t* kq;        // [U][cap][d]
     __half* ks;        // [U][cap][d/32]
-    uint8_t* vc;       // [U][cap][3d/8]
+    uint8_t* vc;       // [U][cap/32][d][12]: per 32-token group and coordinate, one 12-byte code string
     __half* vn;        // [U][cap]
     uint32_t* status;  // status word (bit 0: a bounded device wait gave up)
     float* nmax;       // [U] running maximum of ||v|| per unit
@@ -80,6 +80,13 @@ size_t attend_tc_workspace(const PoolView& p, int rows, int64_t n_ctx);
 polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
                                int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
                                cudaStream_t stream, const SuffixArgs* sfx = nullptr);
+
+// warp-level attention path for few rows per kv head (head_dim 64 with up to 8 rows, 128 with up to 4)
+bool attend_warp_supported(const PoolView& p, int rows);
+size_t attend_warp_workspace(const PoolView& p, int rows, int64_t n_ctx);
+polykv_status launch_attend_warp(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
+                                 int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream, const SuffixArgs* sfx = nullptr);
 
 __host__ __device__ inline float centroid_of(int code) {
     // ascending codes 0..7 -> -c7 .. -c4, c4 .. c7

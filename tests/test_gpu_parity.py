@@ -70,10 +70,11 @@ def check_encode(pool, ref, n_tok, t_off=0, b32=None):
         assert np.array_equal(f["v_packed"][:, :, t_off // 32:t_off // 32 + ng], ref["v_packed"][:, :, :ng])
 
 
-@pytest.fixture(params=["default", "simt"])
+@pytest.fixture(params=["default", "simt", "tc"])
 def path(request):
-    """Attention kernel selection: the library's default (tensor cores for head_dim 128)
-    and the CUDA-core path forced through POLYKV_ATTEND_PATH."""
+    """Attention kernel selection: the library's default (the warp-level kernel for few rows per kv
+    head, the tensor-core kernel for head_dim 128 and more rows), the CUDA-core path, and the
+    tensor-core path where it applies, forced through POLYKV_ATTEND_PATH."""
     old = os.environ.get("POLYKV_ATTEND_PATH")
     if request.param == "default":
         os.environ.pop("POLYKV_ATTEND_PATH", None)
@@ -119,11 +120,11 @@ def run_case(env, L, H, Hq, d, T, A, dtype, seed=0, q_mult=1.0, n_ctx=None, laye
 
 
 # ---- the pages' model shapes
-def test_smollm2_single_layer_600(env):
+def test_smollm2_single_layer_600(env, path):
     run_case(env, 1, 32, 32, 64, 600, 1, "f16")
 
 
-def test_smollm2_full_stack_1851_5_agents(env):
+def test_smollm2_full_stack_1851_5_agents(env, path):
     run_case(env, 24, 32, 32, 64, 1851, 5, "f16", layers=[0, 5, 11, 23])
 
 
@@ -145,6 +146,28 @@ def test_ragged_lengths(env, path, T, d):
 @pytest.mark.parametrize("A,G", [(1, 1), (2, 4), (15, 4), (20, 4), (33, 2), (7, 1)])
 def test_rows_per_kv_head(env, path, A, G):
     run_case(env, 2, 2, 2 * G, 128, 200, A, "bf16", seed=A)
+
+
+# ---- the warp-level kernel (few rows per kv head): every row count it takes, ragged tails,
+# ranges that cross unit boundaries (full layer stacks), peaky queries
+@pytest.mark.parametrize("T", [1, 31, 33, 65, 129, 257, 1000])
+@pytest.mark.parametrize("d,A,G", [(64, 1, 1), (64, 5, 1), (64, 8, 1), (64, 2, 4), (128, 1, 1), (128, 1, 4),
+                                   (128, 2, 2)])
+def test_few_rows_ragged(env, d, A, G, T):
+    run_case(env, 2, 3, 3 * G, d, T, A, "f16" if d == 64 else "bf16", seed=T + 7 * A)
+
+
+def test_few_rows_llama3_8b_4096_one_agent(env, path):
+    run_case(env, 32, 8, 32, 128, 4096, 1, "bf16", layers=[0, 17, 31])
+
+
+def test_few_rows_smollm2_eight_agents_bf16(env):
+    run_case(env, 24, 32, 32, 64, 1851, 8, "bf16", layers=[3, 23])
+
+
+@pytest.mark.parametrize("d,A,G", [(64, 5, 1), (128, 1, 4)])
+def test_few_rows_very_peaky(env, path, d, A, G):
+    run_case(env, 4, 8, 8 * G, d, 1500, A, "f16" if d == 64 else "bf16", q_mult=40.0)
 
 
 def test_peaky_queries_online_rescale(env, path):
