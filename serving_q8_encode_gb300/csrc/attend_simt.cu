@@ -16,6 +16,7 @@
 #include <cmath>
 
 #include "polykv_internal.cuh"
+#include "merge_row.cuh"
 
 namespace polykv {
 namespace {
@@ -263,21 +264,6 @@ __global__ void __launch_bounds__(kThreads) attend_partial_simt(PoolView p, cons
 constexpr int kMergeBatch = 4;
 constexpr int kMergeWarps = 8;
 
-template <int D>
-struct MergeVec;
-template <>
-struct MergeVec<128> {
-    using T = float4;
-    static __device__ __forceinline__ void to(const T& v, float* o) { o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w; }
-    static __device__ __forceinline__ T from(const float* o) { return make_float4(o[0], o[1], o[2], o[3]); }
-};
-template <>
-struct MergeVec<64> {
-    using T = float2;
-    static __device__ __forceinline__ void to(const T& v, float* o) { o[0] = v.x; o[1] = v.y; }
-    static __device__ __forceinline__ T from(const float* o) { return make_float2(o[0], o[1]); }
-};
-
 // First tile-range index overlapping tile position x of the (unit, tile) list
 // cut into nc ranges of tt tiles: floor((x * nc - 1) / tt) for x >= 1. Uses
 // 32-bit division when the product fits, which is the usual case.
@@ -285,50 +271,6 @@ __device__ __forceinline__ int64_t merge_range_of(int64_t x, int nc, int64_t tt)
     const int64_t num = x * nc - 1;
     if (num <= 0xFFFFFFFFll && tt <= 0xFFFFFFFFll) return (int64_t)((uint32_t)num / (uint32_t)tt);
     return num / tt;
-}
-
-// Finishes one output row from its merged rotated-basis accumulator o (this lane's D/32 elements),
-// running maximum M and sum L: the inverse FWHT (1/D) H o, then the private suffix's partial (already
-// in the original basis) under the same softmax, then the division by the total sum.
-template <int D>
-__device__ __forceinline__ void finish_row(float (&o)[D / 32], float M, float L, float2 sml,
-                                           const typename MergeVec<D>::T& sv, int lane) {
-    constexpr int EPL = D / 32;
-    using V = MergeVec<D>;
-    // in-lane butterflies (strides < EPL), then across lanes
-#pragma unroll
-    for (int h = 1; h < EPL; h <<= 1)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e)
-            if ((e & h) == 0) {
-                const float x = o[e], y = o[e + h];
-                o[e] = x + y;
-                o[e + h] = x - y;
-            }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const float other = __shfl_xor_sync(0xffffffffu, o[e], m);
-            o[e] = upper ? other - o[e] : o[e] + other;
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] *= (1.0f / D);
-    if (sml.x != -INFINITY) {
-        // the suffix partial is already in the original basis
-        const float Mn = fmaxf(M, sml.x);
-        const float c = exp2f(M - Mn), w = exp2f(sml.x - Mn);
-        float x[EPL];
-        V::to(sv, x);
-        L = fmaf(w, sml.y, L * c);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, x[e], o[e] * c);
-    }
-    const float inv = 1.0f / L;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] *= inv;
 }
 
 template <int D>
@@ -569,7 +511,8 @@ polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (lay.nc > 0) {
+    if (lay.nc > 0 && lay.RS > 8) {
+        // many rows per segment and few pieces (the tensor-core partition): four rows per warp
         constexpr int rows_per_block = kMergeWarps * kMergeRowsPerWarp;
         cfg.gridDim = dim3((unsigned)((int64_t)U * lay.nrg), (unsigned)((lay.RS + rows_per_block - 1) / rows_per_block));
         e = D == 128 ? cudaLaunchKernelEx(&cfg, attend_merge_tc<128>, ws_acc, ws_ml, out, H, A, Hq, R, lay, sfx_acc, sfx_ml)

@@ -19,7 +19,7 @@
 // copies (one elected lane, one mbarrier per stage), and keeps its softmax
 // state and output accumulator in registers. A range that crosses a unit
 // boundary writes one partial per piece (slot = unit + warp range), which the
-// merge kernel combines.
+// merge kernel combines (log-sum-exp, one inverse FWHT per row).
 //
 // Both contractions of a group run as warp-level m16n8k16 tensor-core MMAs
 // (fp16 operands, fp32 accumulate) held entirely in registers:
@@ -77,11 +77,11 @@ struct WCfg {
 
 struct WParams {
     PoolView p;
-    const uint16_t* q;   // [L][A][Hq][D]
-    float* ws_acc;       // [slots][R][D]
-    float* ws_ml;        // [slots][R][2]
-    int64_t n_ctx, ng, tt;
-    int nw, A, Hq, G, R;
+    const uint16_t* q;       // [L][A][Hq][D]
+    float* ws_acc;           // [slots][R][D]
+    float* ws_ml;            // [slots][R][2]
+    int64_t n_ctx, tt;
+    int ng, nw, A, Hq, G, R;
     float scale_log2;
 };
 
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
 
-    // lane-replicated table of centroid pairs: entry e = (C[e & 7], C[e >> 3]) in fp16
+    // lane-replicated table of centroid pairs: entry e = (C[e & 7], C[e >> 3]) in fp16, lane l's copy of
+    // entry e at byte (32 e + l) * 4
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem);
     for (int e = threadIdx.x; e < 64 * 32; e += blockDim.x) {
         const int idx = e >> 5;
@@ -167,23 +168,46 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
     const int64_t gw = (int64_t)blockIdx.x * C::WARPS + warp;
     if (gw >= P.nw) return;
     const int64_t x0 = gw * P.tt / P.nw, x1 = (gw + 1) * P.tt / P.nw;
-    const int64_t n = x1 - x0;
+    const int n = (int)(x1 - x0);
+    const int64_t u_first = x0 / P.ng;
+    const int64_t u_last = (x1 - 1) / P.ng;
     const uint32_t ring_u = tc::smem_u32(ring);
-    const uint32_t lut_u = tc::smem_u32(lut) + 4u * (uint32_t)lane;
+    const uint32_t lut_u = tc::smem_u32(lut);
+    const uint32_t lane4 = 4u * (uint32_t)lane;
 
-    auto issue = [&](int64_t x, int s) {
-        const int64_t unit = x / P.ng, gi = x - unit * P.ng;
-        const int64_t tok = unit * P.p.cap + gi * kGroup;
+    // streaming cursor (lane 0): pointers to the next group's four fields, advanced one group at a time
+    int igi = (int)(x0 - u_first * P.ng);
+    const int64_t skip = P.p.cap - (int64_t)P.ng * kGroup;   // tokens from a unit's last group to the next unit
+    const int64_t tok_first = u_first * P.p.cap + (int64_t)igi * kGroup;
+    const int8_t* pk = P.p.kq + tok_first * D;
+    const __half* ps = P.p.ks + tok_first * C::NB;
+    const uint8_t* pc = P.p.vc + tok_first * (3 * D / 8);
+    const __half* pn = P.p.vn + tok_first;
+    auto issue_next = [&](int s) {
         const uint32_t dst = ring_u + (uint32_t)(s * C::STAGE);
         const uint32_t bar = tc::smem_u32(&bars[s]);
         tc::mbar_arrive_expect_tx(bar, C::STAGE);
-        tc::bulk_g2s(dst, P.p.kq + tok * D, C::KEY, bar);
-        tc::bulk_g2s(dst + C::KEY, P.p.ks + tok * C::NB, C::SCL, bar);
-        tc::bulk_g2s(dst + C::KEY + C::SCL, P.p.vc + unit * P.p.cap * (3 * D / 8) + gi * C::VCB, C::VCB, bar);
-        tc::bulk_g2s(dst + C::KEY + C::SCL + C::VCB, P.p.vn + tok, C::NRM, bar);
+        tc::bulk_g2s(dst, pk, C::KEY, bar);
+        tc::bulk_g2s(dst + C::KEY, ps, C::SCL, bar);
+        tc::bulk_g2s(dst + C::KEY + C::SCL, pc, C::VCB, bar);
+        tc::bulk_g2s(dst + C::KEY + C::SCL + C::VCB, pn, C::NRM, bar);
+        pk += kGroup * D;
+        ps += kGroup * C::NB;
+        pc += C::VCB;
+        pn += kGroup;
+        if (++igi == P.ng) {
+            igi = 0;
+            pk += skip * D;
+            ps += skip * C::NB;
+            pc += skip * (3 * D / 8);
+            pn += skip;
+        }
     };
     if (lane == 0)
-        for (int k = 0; k < C::STAGES && k < n; ++k) issue(x0 + k, k);
+        for (int k = 0; k < C::STAGES && k < n; ++k) issue_next(k);
+
+    // the norm maxima of this warp's units (at most a few), one per lane, fetched while the first copies fly
+    const float nm_lane = u_first + lane <= u_last ? P.p.nmax[u_first + lane] : 0.0f;
     __syncwarp();
 
     // lane roles: score rows m = g and g + 8 are (row g % RP, block g / RP) and (row g % RP, block g / RP + 8 / RP);
@@ -191,31 +215,33 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
     const int r_lane = g % C::RP;
     const int b_lo = g / C::RP, b_hi = b_lo + 8 / C::RP;
     const int bt = (t * D / 4) / 32;
+    // key row of token 8(g/2) + 2i + g%2 (n-tile i), bytes from t D/4
+    const uint32_t koff = (uint32_t)((8 * (g >> 1) + (g & 1)) * D + t * (D / 4));
     // value strings: this lane's 24-bit field is bytes [3t, 3t+3) of each 12-byte string
     const uint32_t vword = (uint32_t)((3 * t) & ~3);
     const uint32_t vsel = (uint32_t)(((3 * t) & 3) | ((((3 * t) & 3) + 1) << 4) | ((((3 * t) & 3) + 2) << 8));
     // scale pair selector (d = 128): blocks b_lo and b_hi of a token's four
     const uint32_t ssel = (b_lo & 1) ? 0x7632u : 0x5410u;
+    const int rem = (int)(P.n_ctx - (int64_t)(P.ng - 1) * kGroup);   // valid tokens of a unit's last group
 
-    int64_t unit = x0 / P.ng, gi = x0 - unit * P.ng;
+    int64_t unit = u_first;
+    int gi = (int)(x0 - u_first * P.ng);
     float m_run = -INFINITY, crow = 0.0f, wsc = 1.0f;
     float2 lsum = make_float2(0.0f, 0.0f);
     float o[C::MT][4];
     uint32_t qa[C::KS][4];
     bool fresh = true;   // the segment's state must be (re)initialised
     bool aborted = false;
-    int64_t k = 0;
+    int k = 0;
 
-    auto flush = [&](int64_t u) {
-        // (m, l) of row r_lane: sum of the quad's partial sums
+    // end of a segment piece: write this warp's partial (the merge kernel combines the unit's pieces)
+    auto finish_piece = [&](int64_t u) {
         float l = lsum.x + lsum.y;
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
         const int64_t slot = u + gw;   // segment = unit (one row group), piece = this warp's range
-        if (t == 0 && g < C::RP && g < P.R) {
-            P.ws_ml[(slot * P.R + g) * 2] = m_run;
-            P.ws_ml[(slot * P.R + g) * 2 + 1] = l;
-        }
+        if (t == 0 && g < C::RP && g < P.R)
+            reinterpret_cast<float2*>(P.ws_ml)[slot * P.R + g] = make_float2(m_run, l);
         const float iw = 1.0f / wsc;
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt)
@@ -279,7 +305,9 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
                 qa[ks][2] = b_lo == bt ? u23 : 0u;
                 qa[ks][3] = b_hi == bt ? u23 : 0u;
             }
-            wsc = value_wscale(P.p.nmax[unit]);
+            const int64_t ju = unit - u_first;
+            const float nm = __shfl_sync(0xffffffffu, nm_lane, (int)(ju & 31));
+            wsc = value_wscale(ju < 32 ? nm : P.p.nmax[unit]);
             m_run = -INFINITY;
             lsum = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -287,8 +315,8 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             fresh = false;
         }
 
-        const int s = (int)(k % C::STAGES);
         // bounded wait; the outcome is made warp-uniform (and the warp converged) before the MMAs
+        const int s = k % C::STAGES;
         const bool ok = tc::mbar_wait(tc::smem_u32(&bars[s]), (uint32_t)((k / C::STAGES) & 1), &abort_flag, kWaitNs);
         if (!__all_sync(0xffffffffu, ok)) {
             aborted = true;
@@ -296,16 +324,14 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
         }
         const uint32_t st = ring_u + (uint32_t)(s * C::STAGE);
 
-        // ---- scores of this lane's row for tokens 8t + 2i + {0, 1}, i = 0..3
+        // ---- scores: S^T[(row, block)][token] for tokens 8t + 2i + {0, 1} of this lane's row, n-tile i
         float sc[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
-            const int tok = 8 * (g >> 1) + 2 * i + (g & 1);
-            const uint32_t krow = st + (uint32_t)(tok * D + t * (D / 4));
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
-                const uint4 w = lds128(krow + 16u * c);
+                const uint4 w = lds128(st + koff + (uint32_t)(2 * i * D + 16 * c));
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -320,7 +346,7 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
         float2 s_lo[4], s_hi[4], nw[4];   // per token pair (2i, 2i+1): scale of block b_lo / b_hi, norm * w
         {
             const uint32_t sbase = st + C::KEY + (uint32_t)(t * 8 * C::NB * 2);
-            uint32_t sw[8];   // per token: (scale b_lo, scale b_hi) as fp16 pair
+            uint32_t sw[8];   // per token: (scale b_lo, scale b_hi) as an fp16 pair
             if constexpr (C::NB == 2) {
                 const uint4 a = lds128(sbase), b = lds128(sbase + 16);
                 sw[0] = a.x; sw[1] = a.y; sw[2] = a.z; sw[3] = a.w;
@@ -328,25 +354,25 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint4 a = lds128(sbase + 16u * c);   // tokens 2c, 2c+1: 4 scales each
+                    const uint4 a = lds128(sbase + 16u * c);   // tokens 2c, 2c+1: four scales each
                     sw[2 * c] = __byte_perm(a.x, a.y, ssel);
                     sw[2 * c + 1] = __byte_perm(a.z, a.w, ssel);
                 }
             }
             const uint4 nv = lds128(st + C::KEY + C::SCL + C::VCB + (uint32_t)(t * 16));
             const uint32_t nws[4] = {nv.x, nv.y, nv.z, nv.w};
-            const float2 cr = make_float2(crow, crow), wv = make_float2(wsc, wsc);
+            const __half2 wh = __float2half2_rn(wsc);   // a power of two: exact, and ||v|| w < 2^7
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t plo = __byte_perm(sw[2 * i], sw[2 * i + 1], 0x5410);
                 const uint32_t phi = __byte_perm(sw[2 * i], sw[2 * i + 1], 0x7632);
-                s_lo[i] = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&plo)), cr);
-                s_hi[i] = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&phi)), cr);
-                nw[i] = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&nws[i])), wv);
+                s_lo[i] = __half22float2(*reinterpret_cast<const __half2*>(&plo));
+                s_hi[i] = __half22float2(*reinterpret_cast<const __half2*>(&phi));
+                nw[i] = __half22float2(__hmul2(*reinterpret_cast<const __half2*>(&nws[i]), wh));
             }
         }
 
-        // logits in log2 units (absolute, then relative to the running maximum)
+        // scores with the block scales applied (the row's logit scale is applied with the maximum below)
         float2 y[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -357,27 +383,32 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
                 y[i].y += __shfl_xor_sync(0xffffffffu, y[i].y, 16);
             }
         }
-        if (gi * kGroup + kGroup > P.n_ctx) {   // the unit's ragged last group: no weight past n_ctx
-            const int64_t tok0 = gi * kGroup + 8 * t;
+        if (gi == P.ng - 1 && rem < kGroup) {   // the unit's ragged last group: no weight past n_ctx
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if (tok0 + 2 * i >= P.n_ctx) { y[i].x = -INFINITY; nw[i].x = 0.0f; }
-                if (tok0 + 2 * i + 1 >= P.n_ctx) { y[i].y = -INFINITY; nw[i].y = 0.0f; }
+                if (8 * t + 2 * i >= rem) { y[i].x = -INFINITY; nw[i].x = 0.0f; }
+                if (8 * t + 2 * i + 1 >= rem) { y[i].y = -INFINITY; nw[i].y = 0.0f; }
             }
         }
+        // logits in log2 units relative to the running maximum: y * crow - m
+        const float2 cr = make_float2(crow, crow);
         float2 xl[4];
         {
             const float2 negm = make_float2(-m_run, -m_run);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xl[i] = __fadd2_rn(y[i], negm);
+            for (int i = 0; i < 4; ++i) xl[i] = __ffma2_rn(y[i], cr, negm);
         }
         const float xm = fmaxf(fmaxf(fmaxf(xl[0].x, xl[0].y), fmaxf(xl[1].x, xl[1].y)),
                                fmaxf(fmaxf(xl[2].x, xl[2].y), fmaxf(xl[3].x, xl[3].y)));
         if (__any_sync(0xffffffffu, xm > 8.0f)) {
             // rare (always on a segment's first group): raise each row's running maximum to at least the
             // group's, rescale what the row has accumulated, and redo the relative logits
-            float gm = fmaxf(fmaxf(fmaxf(y[0].x, y[0].y), fmaxf(y[1].x, y[1].y)),
-                             fmaxf(fmaxf(y[2].x, y[2].y), fmaxf(y[3].x, y[3].y)));
+            float gm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 ya = __fmul2_rn(y[i], cr);
+                gm = fmaxf(gm, fmaxf(ya.x, ya.y));
+            }
             gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
             gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
             const float m_new = fmaxf(m_run, gm);
@@ -397,7 +428,7 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             }
             const float2 negm = make_float2(-m_run, -m_run);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xl[i] = __fadd2_rn(y[i], negm);
+            for (int i = 0; i < 4; ++i) xl[i] = __ffma2_rn(y[i], cr, negm);
         }
 
         // probabilities (row sums in fp32) and the value MMA's B fragments P' = p ||v|| w in fp16
@@ -411,7 +442,8 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             pb[i] = *reinterpret_cast<const uint32_t*>(&h);
         }
 
-        // values: coordinates 16 mt + g and 16 mt + g + 8, tokens 8t .. 8t+7 (k-step j: 8t + 4j + {0, 1, 2, 3})
+        // values: coordinates 16 mt + g and 16 mt + g + 8, tokens 8t .. 8t+7 (k-step j: 8t + 4j + {0, 1, 2, 3});
+        // a pair's table offset keeps the lane's byte offset in its low bits
         const uint32_t vbase = st + (uint32_t)(C::KEY + C::SCL) + vword;
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
@@ -419,37 +451,37 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             const uint32_t fa = __byte_perm(lds32(pa), lds32(pa + 4u), vsel);
             const uint32_t fb = __byte_perm(lds32(pa + 96u), lds32(pa + 100u), vsel);
             uint32_t a[4];
-            a[0] = lds32(lut_u + pair_offset<0>(fa));
-            a[1] = lds32(lut_u + pair_offset<0>(fb));
-            a[2] = lds32(lut_u + pair_offset<6>(fa));
-            a[3] = lds32(lut_u + pair_offset<6>(fb));
+            a[0] = lds32(lut_u + (pair_offset<0>(fa) | lane4));
+            a[1] = lds32(lut_u + (pair_offset<0>(fb) | lane4));
+            a[2] = lds32(lut_u + (pair_offset<6>(fa) | lane4));
+            a[3] = lds32(lut_u + (pair_offset<6>(fb) | lane4));
             mma16816(o[mt], a, pb[0], pb[1]);
-            a[0] = lds32(lut_u + pair_offset<12>(fa));
-            a[1] = lds32(lut_u + pair_offset<12>(fb));
-            a[2] = lds32(lut_u + pair_offset<18>(fa));
-            a[3] = lds32(lut_u + pair_offset<18>(fb));
+            a[0] = lds32(lut_u + (pair_offset<12>(fa) | lane4));
+            a[1] = lds32(lut_u + (pair_offset<12>(fb) | lane4));
+            a[2] = lds32(lut_u + (pair_offset<18>(fa) | lane4));
+            a[3] = lds32(lut_u + (pair_offset<18>(fb) | lane4));
             mma16816(o[mt], a, pb[2], pb[3]);
         }
 
         // release the stage (generic reads ordered before the async-proxy refill) and refill it
         tc::fence_proxy_async();
         __syncwarp();
-        if (lane == 0 && k + C::STAGES < n) issue(x0 + k + C::STAGES, s);
+        if (lane == 0 && k + C::STAGES < n) issue_next(s);
 
         if (++gi == P.ng) {
-            flush(unit);
+            finish_piece(unit);
             ++unit;
             gi = 0;
             fresh = true;
         }
     }
     if (!aborted) {
-        if (!fresh) flush(unit);
+        if (!fresh) finish_piece(unit);
         return;
     }
     // gave up on a wait: let this warp's copies in flight land (bounded) before the CTA can exit
-    const int64_t last = k + C::STAGES < n ? k + C::STAGES : n;
-    for (int64_t j = k; j < last; ++j) {
+    const int last = k + C::STAGES < n ? k + C::STAGES : n;
+    for (int j = k; j < last; ++j) {
         const uint32_t bar = tc::smem_u32(&bars[j % C::STAGES]);
         const uint32_t par = (uint32_t)((j / C::STAGES) & 1);
         const uint64_t t0 = tc::globaltimer();
@@ -487,22 +519,28 @@ WPlan<D> wplan(const PoolView& p, int64_t n_ctx) {
     return pl;
 }
 
+template <int D>
+size_t warp_workspace(const WPlan<D>& pl, int R) {
+    return sizeof(float) * pl.slots * (size_t)R * (size_t)(D + 2);
+}
+
 template <int D, bool BF16>
 polykv_status run_warp(const PoolView& p, const void* q, float* out, int A, int Hq, int64_t n_ctx, float scale,
                        void* ws, size_t ws_bytes, cudaStream_t stream, const SuffixArgs* sfx) {
     using C = WCfg<D>;
     const int G = Hq / p.H, R = A * G;
     const WPlan<D> pl = wplan<D>(p, n_ctx);
-    const size_t need = sizeof(float) * pl.slots * (size_t)R * (size_t)(D + 2);
+    const size_t need = warp_workspace<D>(pl, R);
     if (ws_bytes < need) return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend: workspace %zu < %zu bytes", ws_bytes, need);
+    if (pl.ng > 0x7FFFFFFF) return set_error(POLYKV_E_UNSUPPORTED, "attend: context too long");
     WParams P;
     P.p = p;
     P.q = static_cast<const uint16_t*>(q);
     P.ws_acc = static_cast<float*>(ws);
     P.ws_ml = P.ws_acc + pl.slots * (size_t)R * D;
     P.n_ctx = n_ctx;
-    P.ng = pl.ng;
     P.tt = pl.tt;
+    P.ng = (int)pl.ng;
     P.nw = pl.nw;
     P.A = A;
     P.Hq = Hq;
@@ -536,8 +574,7 @@ bool attend_warp_supported(const PoolView& p, int rows) {
 }
 
 size_t attend_warp_workspace(const PoolView& p, int rows, int64_t n_ctx) {
-    const size_t slots = p.d == 64 ? wplan<64>(p, n_ctx).slots : wplan<128>(p, n_ctx).slots;
-    return sizeof(float) * slots * (size_t)rows * (size_t)(p.d + 2);
+    return p.d == 64 ? warp_workspace<64>(wplan<64>(p, n_ctx), rows) : warp_workspace<128>(wplan<128>(p, n_ctx), rows);
 }
 
 polykv_status launch_attend_warp(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
