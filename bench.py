@@ -59,6 +59,9 @@ def measured_bf16_tflops():
     return 1900.0
 
 
+ATTEND_SOURCES = ["attend_tc.cu", "attend_warp.cu", "attend_simt.cu", "attend_suffix.cu", "merge_row.cuh"]
+
+
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -185,22 +188,32 @@ def whole_job_gbs(world: int, bytes_per_rank: float, ms: float) -> float:
 
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, w: synth.Workload):
-    """The CPU oracle, timed as it stands, on a bounded sample per step."""
+    """The CPU oracle, timed as it stands, on a bounded sample per step: one layer and two kv heads
+    (all their tokens, agents and query heads, and the private suffix when the workload has one),
+    scaled to the whole workload's algorithmic bytes."""
     import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     c32, b32 = oracle.codebook.codebook_f32()
-    sample_layers = 1
-    kb, vb = synth.gen_kv(sample_layers, w.n_kv_heads, w.n_ctx, w.head_dim, w.dtype, 0)
-    qb = synth.gen_q(sample_layers, w.n_agents, w.n_q_heads, w.head_dim, w.dtype, 0)
+    heads = min(2, w.n_kv_heads)
+    G = w.n_q_heads // w.n_kv_heads
+    kb, vb = synth.gen_kv(1, w.n_kv_heads, w.n_ctx, w.head_dim, w.dtype, 0)
+    qb = synth.gen_q(1, w.n_agents, w.n_q_heads, w.head_dim, w.dtype, 0)
+    kb, vb = kb[:, :heads], vb[:, :heads]
+    qb = np.ascontiguousarray(qb[:, :, :heads * G])
+    sfx = {}
+    if w.suffix_len:
+        skb, svb = synth.gen_suffix(1, w.n_agents, w.n_kv_heads, w.suffix_len, w.head_dim, w.dtype, 0)
+        sfx = dict(suffix_k_bits=np.ascontiguousarray(skb[:, :, :heads]),
+                   suffix_v_bits=np.ascontiguousarray(svb[:, :, :heads]))
     enc_b, att_b = algorithmic_bytes(w, w.n_ctx, w.n_agents)
-    frac = sample_layers / w.n_layers
+    frac = heads / (w.n_layers * w.n_kv_heads)
     sample_bytes = (enc_b + att_b) * frac
 
     def step():
         pool = oracle.attention.encode_pool(kb, vb, w.dtype, b32)
-        oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32)
+        oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32, **sfx)
 
     for _ in range(args.warmup):
         step()
@@ -214,10 +227,10 @@ def run_reference(args, w: synth.Workload):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(w.describe(), sample=f"{sample_layers} of {w.n_layers} layers per step"),
+        "config": dict(w.describe(), sample=f"1 of {w.n_layers} layers x {heads} of {w.n_kv_heads} kv heads per step"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"encode + attend of {sample_layers} layer(s) x {w.n_kv_heads} kv heads x "
-                                   f"{w.n_ctx} tokens x {w.n_agents} agents per step; numpy (BLAS may thread)"},
+                         "sample": f"encode + attend of 1 layer x {heads} kv heads x {w.n_ctx} tokens x "
+                                   f"{w.n_agents} agents per step; numpy (BLAS may thread)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -226,17 +239,21 @@ def run_reference(args, w: synth.Workload):
 
 def _oracle_layer(job):
     """One layer of the workload through the CPU oracle, encode and attend timed separately. Runs in a
-    spawned worker process with one BLAS thread (set by _one_thread before numpy is imported)."""
+    spawned worker process with one BLAS thread (the parent sets the thread counts before spawning)."""
     name, layer_seed, n_layers_override = job
     import oracle
     w = synth.WORKLOADS[name]
     c32, b32 = oracle.codebook.codebook_f32()
     kb, vb = synth.gen_kv(1, w.n_kv_heads, w.n_ctx, w.head_dim, w.dtype, layer_seed)
     qb = synth.gen_q(1, w.n_agents, w.n_q_heads, w.head_dim, w.dtype, layer_seed)
+    sfx = {}
+    if w.suffix_len:
+        skb, svb = synth.gen_suffix(1, w.n_agents, w.n_kv_heads, w.suffix_len, w.head_dim, w.dtype, layer_seed)
+        sfx = dict(suffix_k_bits=skb, suffix_v_bits=svb)
     t0 = time.perf_counter()
     pool = oracle.attention.encode_pool(kb, vb, w.dtype, b32)
     t1 = time.perf_counter()
-    oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32)
+    oracle.attention.attend_pool(qb, w.dtype, pool, w.n_ctx, c32, **sfx)
     t2 = time.perf_counter()
     return t1 - t0, t2 - t1
 
@@ -420,11 +437,10 @@ def run_polykv(args, w: synth.Workload):
     if dominant == "encode":
         kname, kbytes, kms, files = "encode_kernel", enc_b, enc_ms_m, ["encode.cu"]
     else:
-        kname, kbytes, kms, files = "attend", att_b, att_ms_m, ["attend_tc.cu", "attend_simt.cu", "attend_suffix.cu"]
+        kname, kbytes, kms, files = "attend", att_b, att_ms_m, ATTEND_SOURCES
     achieved = kbytes / (kms * 1e-3) / 1e9
     traffic = traffic_from_profiles(kname, w.name, kernel_source_hash(files))
-    att_traffic = traffic_from_profiles("attend", w.name,
-                                        kernel_source_hash(["attend_tc.cu", "attend_simt.cu", "attend_suffix.cu"]))
+    att_traffic = traffic_from_profiles("attend", w.name, kernel_source_hash(ATTEND_SOURCES))
     h2d = kb.nbytes + vb.nbytes + qb.nbytes
     d2h = L * A * Hq * d * 4
     if rank != 0:
@@ -464,14 +480,14 @@ def run_sweep(args):
     import serving_q8_encode_gb300 as pk
 
     base = synth.WORKLOADS[DEFAULT_WORKLOAD]
-    L, H, Hq, d = base.n_layers, base.n_kv_heads, base.n_q_heads, base.head_dim
+    L, H, Hq, d = args.layers or base.n_layers, base.n_kv_heads, base.n_q_heads, base.head_dim
     dev = torch.device("cuda", 0)
     peak, peak_src = measured_peaks()
     bf16_peak = measured_bf16_tflops()
     flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
     rows = []
-    for T in (600, 1851, 4096, 7194):
+    for T in args.sweep_ctx:
         kb, vb = synth.gen_kv(L, H, T, d, base.dtype, seed=0)
         k = torch.from_numpy(kb.view(np.int16)).to(dev)
         v = torch.from_numpy(vb.view(np.int16)).to(dev)
@@ -497,7 +513,7 @@ def run_sweep(args):
         enc_us = timed(lambda: pool.encode(k, v, stream=stream), args.steps)
         rows.append({"mode": "encode", "n_ctx": T, "us": enc_us, "tokens_per_s": T / (enc_us * 1e-6),
                      "gbs": enc_b / (enc_us * 1e-6) / 1e9})
-        for A in (1, 2, 4, 8, 15):
+        for A in args.sweep_agents:
             qb = synth.gen_q(L, A, Hq, d, base.dtype, seed=0)
             q = torch.from_numpy(qb.view(np.int16)).to(dev)
             out = torch.empty((L, A, Hq, d), dtype=torch.float32, device=dev)
@@ -538,7 +554,7 @@ def run_sweep(args):
                 torch.cuda.empty_cache()
         del pool, k, v
         torch.cuda.empty_cache()
-    print(json.dumps({"sweep": "llama3_8b shape, encode-only and attend-only", "peak_gbs": peak,
+    print(json.dumps({"sweep": f"llama3_8b shape ({L} layers), encode-only and attend-only", "peak_gbs": peak,
                       "peak_source": peak_src, "bf16_tflops_peak": bf16_peak, "l2": L2Flush.describe,
                       "rows": rows}), flush=True)
     return 0
@@ -557,6 +573,10 @@ def main():
                     help="encode-only / attend-only grid over context {600,1851,4096,7194} x agents {1,2,4,8,15}")
     ap.add_argument("--chunk", type=int, default=0,
                     help="with --sweep: also time query-chunk mode with this many query tokens per agent")
+    ap.add_argument("--sweep-ctx", type=lambda x: [int(v) for v in x.split(",")], default=[600, 1851, 4096, 7194],
+                    help="with --sweep: comma-separated context lengths")
+    ap.add_argument("--sweep-agents", type=lambda x: [int(v) for v in x.split(",")], default=[1, 2, 4, 8, 15],
+                    help="with --sweep: comma-separated agent counts")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (smaller cases for profiler captures)")
     args = ap.parse_args()
