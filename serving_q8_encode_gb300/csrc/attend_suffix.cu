@@ -17,22 +17,42 @@
 namespace polykv {
 namespace {
 
-constexpr int kSfxTile = 128;   // suffix tokens per tile (one per thread)
+constexpr int kSfxTile = 128;   // suffix tokens per tile (one per thread for the scores)
 constexpr int kSfxThreads = 128;
 
 __device__ __forceinline__ float bits_to_float(uint16_t b, bool bf16) {
     return bf16 ? __uint_as_float((uint32_t)b << 16) : __half2float(__ushort_as_half(b));
 }
 
-// grid: one block per (layer, agent, kv head); block: 128 threads.
+// Shared-memory tile of the suffix: keys with rows padded by 16 bytes (a thread reads its token's row;
+// the padding spreads eight consecutive rows over distinct banks) and values unpadded (a thread reads
+// one column; consecutive threads read consecutive 2-byte elements).
+template <int D>
+struct SfxTileSmem {
+    static constexpr int kKRow = 2 * D + 16;
+    static constexpr int kKBytes = kSfxTile * kKRow;
+    static constexpr int kVBytes = kSfxTile * 2 * D;
+    static constexpr int kBytes = kKBytes + kVBytes;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// grid: one block per (layer, agent, kv head); block: 128 threads. Each 128-token tile of the agent's
+// keys and values is copied into shared memory with coalesced 16-byte asynchronous copies; the scores
+// (thread = token) and the value accumulation (thread = head dim) then read shared memory only.
 template <int D, int GMAX, bool BF16>
 __global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __restrict__ q,
                                                               const uint16_t* __restrict__ sk,
                                                               const uint16_t* __restrict__ sv, int A, int H, int Hq,
                                                               int64_t S, float scale_log2, float* __restrict__ acc_out,
                                                               float* __restrict__ ml_out) {
-    __shared__ float qs[GMAX][D];
-    __shared__ float ps[GMAX][kSfxTile + 1];
+    using T = SfxTileSmem<D>;
+    extern __shared__ __align__(16) unsigned char sfx_smem[];
+    __shared__ __align__(16) float qs[GMAX][D];
+    __shared__ __align__(16) float ps[kSfxTile][GMAX];   // probabilities, token-major
     __shared__ float red[4][GMAX];
     __shared__ float m_s[GMAX], l_s[GMAX], al_s[GMAX];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -42,6 +62,9 @@ __global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __
     const int la = unit / H;                        // layer * A + a
     const uint16_t* kbase = sk + (int64_t)unit * S * D;
     const uint16_t* vbase = sv + (int64_t)unit * S * D;
+    const uint32_t ks_u = (uint32_t)__cvta_generic_to_shared(sfx_smem);
+    const uint32_t vs_u = ks_u + T::kKBytes;
+    const uint16_t* Vs = reinterpret_cast<const uint16_t*>(sfx_smem + T::kKBytes);
 
     for (int i = tid; i < GMAX * D; i += kSfxThreads) {
         const int g = i / D, j = i % D;
@@ -51,35 +74,57 @@ __global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __
         m_s[tid] = -INFINITY;
         l_s[tid] = 0.0f;
     }
-    // accumulator: column j = tid (and tid + 128 / 64 rows split for D = 64 handled by the loop)
-    constexpr int CPT = (D + kSfxThreads - 1) / kSfxThreads;   // columns per thread
+    constexpr int CPT = (D + kSfxThreads - 1) / kSfxThreads;   // accumulator columns per thread
     float acc[GMAX][CPT];
 #pragma unroll
     for (int g = 0; g < GMAX; ++g)
 #pragma unroll
         for (int c = 0; c < CPT; ++c) acc[g][c] = 0.0f;
-    __syncthreads();
 
+    constexpr int kChunksPerRow = D / 8;            // 16-byte chunks per key or value row
     for (int64_t t0 = 0; t0 < S; t0 += kSfxTile) {
-        // scores: thread = token
-        const int64_t t = t0 + tid;
-        const bool valid = t < S;
+        const int tmax = (int)((S - t0) < kSfxTile ? (S - t0) : kSfxTile);
+        // ---- the tile's keys and values into shared memory (rows past the suffix are not copied)
+        for (int c = tid; c < tmax * kChunksPerRow; c += kSfxThreads) {
+            const int row = c / kChunksPerRow, col = c - row * kChunksPerRow;
+            const int64_t goff = (t0 + row) * D + col * 8;
+            cp_async16(ks_u + (uint32_t)(row * T::kKRow + col * 16), kbase + goff);
+            cp_async16(vs_u + (uint32_t)(row * 2 * D + col * 16), vbase + goff);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+
+        // ---- scores: thread = token
+        const bool valid = tid < tmax;
         float x[GMAX];
 #pragma unroll
         for (int g = 0; g < GMAX; ++g) x[g] = 0.0f;
         if (valid) {
-            const uint4* krow = reinterpret_cast<const uint4*>(kbase + t * D);
+            const unsigned char* krow = sfx_smem + tid * T::kKRow;
 #pragma unroll 4
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 w = krow[c];
+            for (int c = 0; c < kChunksPerRow; ++c) {
+                const uint4 w = *reinterpret_cast<const uint4*>(krow + 16 * c);
                 const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                float kf[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float k0 = bits_to_float((uint16_t)(wv[e] & 0xFFFFu), BF16);
-                    const float k1 = bits_to_float((uint16_t)(wv[e] >> 16), BF16);
-                    const int j = 8 * c + 2 * e;
+                    kf[2 * e] = bits_to_float((uint16_t)(wv[e] & 0xFFFFu), BF16);
+                    kf[2 * e + 1] = bits_to_float((uint16_t)(wv[e] >> 16), BF16);
+                }
 #pragma unroll
-                    for (int g = 0; g < GMAX; ++g) x[g] = fmaf(qs[g][j + 1], k1, fmaf(qs[g][j], k0, x[g]));
+                for (int g = 0; g < GMAX; ++g) {
+                    const float4 qa = *reinterpret_cast<const float4*>(&qs[g][8 * c]);
+                    const float4 qb = *reinterpret_cast<const float4*>(&qs[g][8 * c + 4]);
+                    float s = x[g];
+                    s = fmaf(qa.x, kf[0], s);
+                    s = fmaf(qa.y, kf[1], s);
+                    s = fmaf(qa.z, kf[2], s);
+                    s = fmaf(qa.w, kf[3], s);
+                    s = fmaf(qb.x, kf[4], s);
+                    s = fmaf(qb.y, kf[5], s);
+                    s = fmaf(qb.z, kf[6], s);
+                    s = fmaf(qb.w, kf[7], s);
+                    x[g] = s;
                 }
             }
         }
@@ -103,7 +148,7 @@ __global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __
 #pragma unroll
         for (int g = 0; g < GMAX; ++g) {
             const float p = valid ? exp2f(x[g] - m_s[g]) : 0.0f;
-            ps[g][tid] = p;
+            ps[tid][g] = p;
             float v = p;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -111,22 +156,28 @@ __global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __
         }
         __syncthreads();
         if (tid < GMAX) l_s[tid] = l_s[tid] * al_s[tid] + red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
-        // values: thread = column
-        const int tmax = (int)((S - t0) < kSfxTile ? (S - t0) : kSfxTile);
+        // ---- values: thread = column
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
             const int j = tid + c * kSfxThreads;
             if (j < D) {
 #pragma unroll
                 for (int g = 0; g < GMAX; ++g) acc[g][c] *= al_s[g];
+#pragma unroll 4
                 for (int tt = 0; tt < tmax; ++tt) {
-                    const float vv = bits_to_float(vbase[(t0 + tt) * D + j], BF16);
+                    const float vv = bits_to_float(Vs[tt * D + j], BF16);
 #pragma unroll
-                    for (int g = 0; g < GMAX; ++g) acc[g][c] = fmaf(ps[g][tt], vv, acc[g][c]);
+                    for (int g4 = 0; g4 < GMAX; g4 += 4) {
+                        const float4 p4 = *reinterpret_cast<const float4*>(&ps[tt][g4]);
+                        acc[g4][c] = fmaf(p4.x, vv, acc[g4][c]);
+                        acc[g4 + 1][c] = fmaf(p4.y, vv, acc[g4 + 1][c]);
+                        acc[g4 + 2][c] = fmaf(p4.z, vv, acc[g4 + 2][c]);
+                        acc[g4 + 3][c] = fmaf(p4.w, vv, acc[g4 + 3][c]);
+                    }
                 }
             }
         }
-        __syncthreads();
+        __syncthreads();   // the tile's shared memory is reused by the next tile's copies
     }
     // partial per query head hq = h*G + g of agent a
 #pragma unroll
@@ -286,22 +337,26 @@ polykv_status run_chunk(const SuffixArgs& a, int L, int A_virtual, int H, int Hq
     return POLYKV_OK;
 }
 
+template <int D, int GMAX, bool BF16>
+polykv_status launch_suffix_partial(const SuffixArgs& a, int L, int A, int H, int Hq, float sl, cudaStream_t st) {
+    constexpr int smem = SfxTileSmem<D>::kBytes;
+    auto kern = suffix_partial<D, GMAX, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "suffix: smem attribute: %s", cudaGetErrorString(e));
+    const unsigned blocks = (unsigned)((int64_t)L * A * H);
+    kern<<<blocks, kSfxThreads, smem, st>>>(static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
+                                            static_cast<const uint16_t*>(a.v), A, H, Hq, a.len, sl, a.acc, a.ml);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "suffix launch: %s", cudaGetErrorString(e));
+    return POLYKV_OK;
+}
+
 template <int D, bool BF16>
 polykv_status run_suffix(const SuffixArgs& a, int L, int A, int H, int Hq, float scale, cudaStream_t st) {
     const int G = Hq / H;
-    const unsigned blocks = (unsigned)((int64_t)L * A * H);
     const float sl = scale * 1.4426950408889634f;
-    if (G <= 4)
-        suffix_partial<D, 4, BF16><<<blocks, kSfxThreads, 0, st>>>(
-            static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), static_cast<const uint16_t*>(a.v), A,
-            H, Hq, a.len, sl, a.acc, a.ml);
-    else
-        suffix_partial<D, 16, BF16><<<blocks, kSfxThreads, 0, st>>>(
-            static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), static_cast<const uint16_t*>(a.v), A,
-            H, Hq, a.len, sl, a.acc, a.ml);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "suffix launch: %s", cudaGetErrorString(e));
-    return POLYKV_OK;
+    if (G <= 4) return launch_suffix_partial<D, 4, BF16>(a, L, A, H, Hq, sl, st);
+    return launch_suffix_partial<D, 16, BF16>(a, L, A, H, Hq, sl, st);
 }
 
 }  // namespace

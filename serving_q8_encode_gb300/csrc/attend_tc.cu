@@ -469,6 +469,9 @@ __device__ __forceinline__ void write_row_stats(const float2 (&l)[8], Misc& M, i
             ml_slot[2 * r + 1] = (M.red[g][0][lane] + M.red[g][1][lane]) + (M.red[g][2][lane] + M.red[g][3][lane]);
         }
     }
+    // the next segment's first tile rewrites M.red before its own first barrier: no warp of the group may
+    // get there while these sums are still being read
+    tc::named_bar(kBarGroup + g, 128);
 }
 
 template <bool QBF16>
