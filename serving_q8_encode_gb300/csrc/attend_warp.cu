@@ -165,7 +165,9 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
     // the merge may be scheduled now; it waits for this grid's writes before reading them
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    const int64_t gw = (int64_t)blockIdx.x * C::WARPS + warp;
+    // warp ranges are numbered across CTAs first, so that a grid with fewer ranges than warps still
+    // spreads them over every SM
+    const int64_t gw = (int64_t)warp * gridDim.x + blockIdx.x;
     if (gw >= P.nw) return;
     const int64_t x0 = gw * P.tt / P.nw, x1 = (gw + 1) * P.tt / P.nw;
     const int n = (int)(x1 - x0);
@@ -514,7 +516,10 @@ WPlan<D> wplan(const PoolView& p, int64_t n_ctx) {
     pl.tt = (int64_t)p.L * p.H * pl.ng;
     const int64_t warps = (int64_t)sm_count() * C::CTAS * C::WARPS;
     pl.nw = (int)(pl.tt < warps ? pl.tt : warps);
-    pl.nctas = (pl.nw + C::WARPS - 1) / C::WARPS;
+    // ranges are numbered across CTAs first (range = warp * grid + CTA): with one CTA per SM slot even
+    // a small number of ranges is spread over every SM
+    const int64_t slots_ctas = (int64_t)sm_count() * C::CTAS;
+    pl.nctas = (int)(pl.nw < slots_ctas ? pl.nw : slots_ctas);
     pl.slots = (size_t)((int64_t)p.L * p.H + pl.nw);
     return pl;
 }

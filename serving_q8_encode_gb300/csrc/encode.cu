@@ -103,19 +103,6 @@ __device__ __forceinline__ float ge_f32(float a, float b) {
     return r;
 }
 
-// code = number of boundaries b_i * ||v|| <= y. The boundaries are symmetric (b_{6-i} = -b_i,
-// b_3 = 0): with m = #{i in 4..6 : |y| >= t_i}, the code is 4 + m for y >= 0 and 3 - m for y < 0,
-// i.e. 3.5 + copysign(m + 0.5, y). This returns the signed half-code copysign(m + 0.5, y) = code - 3.5
-// as an exact float; the caller adds the 3.5s of a whole group at once. For y < 0 the definition
-// compares |y| > t_i and y = -0 belongs to the upper half; both differences happen only at an exact
-// boundary (|y| equal to a scaled boundary, or u = 0), inside the boundary exemption. Float
-// arithmetic keeps this work on the FMA pipe; the integer/compare pipe is the encoder's bottleneck.
-__device__ __forceinline__ float value_half_code(float y, float t4, float t5, float t6) {
-    const float ay = fabsf(y);
-    const float half_m = ((0.5f + ge_f32(ay, t4)) + ge_f32(ay, t5)) + ge_f32(ay, t6);
-    return copysignf(half_m, y);
-}
-
 // three-input maximum that returns NaN if any input is NaN (a block holding a NaN then gets a NaN
 // scale and all-zero codes, as when the maximum is taken with NaN propagation)
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -290,15 +277,37 @@ __global__ void __launch_bounds__(D, D == 128 ? 8 : 12) encode_kernel(const uint
             y[i + 1] = r.y;
         }
     }
+    // code = number of boundaries b_i * ||v|| <= y. The boundaries are symmetric (b_{6-i} = -b_i,
+    // b_3 = 0): with m = #{i in 4..6 : |y| >= t_i}, the code is 4 + m for y >= 0 and 3 - m for y < 0,
+    // i.e. 3.5 + copysign(m + 0.5, y). The encoder keeps the signed half-code copysign(m + 0.5, y) = code - 3.5
+    // as an exact float and adds the 3.5s of a whole group at once. For y < 0 the definition
+    // compares |y| > t_i and y = -0 belongs to the upper half; both differences happen only at an exact
+    // boundary (|y| equal to a scaled boundary, or u = 0), inside the boundary exemption. Float
+    // arithmetic keeps this work on the FMA pipe; the integer/compare pipe is the encoder's bottleneck.
     // 3-bit decisions in registers: the signed half-code c - 3.5 of every coordinate, an exact float in
     // {+-0.5, +-1.5, +-2.5, +-3.5}; a zero norm gives u = 0 and code 4; a token outside [t0, t0 + n)
     // gets code 0 and keeps its old bits (phase 2)
     {
         const float t4 = __fmul_rn(kB4, nrm), t5 = __fmul_rn(kB5, nrm), t6 = __fmul_rn(kB6, nrm);
-        const float fill = nrm > 0.0f ? 0.0f : 0.5f;   // ||v|| = 0: every code is 4
-        const bool decide = valid && nrm > 0.0f;
+        if (valid && nrm > 0.0f) {
+            // pairs of coordinates: the three 0/1 compares summed with packed adds (exact: small integers
+            // and halves), then the sign of y
+            const float2 half2 = make_float2(0.5f, 0.5f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = decide ? value_half_code(y[i], t4, t5, t6) : (valid ? fill : -3.5f);
+            for (int i = 0; i < 32; i += 2) {
+                const float a0 = fabsf(y[i]), a1 = fabsf(y[i + 1]);
+                float2 h = add2(half2, make_float2(ge_f32(a0, t4), ge_f32(a1, t4)));
+                h = add2(h, make_float2(ge_f32(a0, t5), ge_f32(a1, t5)));
+                h = add2(h, make_float2(ge_f32(a0, t6), ge_f32(a1, t6)));
+                y[i] = copysignf(h.x, y[i]);
+                y[i + 1] = copysignf(h.y, y[i + 1]);
+            }
+        } else {
+            // ||v|| = 0: every code is 4 (half-code 0.5); a token outside [t0, t0 + n): code 0 (-3.5), bits kept
+            const float fv = valid ? 0.5f : -3.5f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = fv;
+        }
     }
     // the half-codes go to shared memory (rotated chunks, see enc_phys)
 #pragma unroll

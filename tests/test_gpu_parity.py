@@ -157,6 +157,17 @@ def test_few_rows_ragged(env, d, A, G, T):
     run_case(env, 2, 3, 3 * G, d, T, A, "f16" if d == 64 else "bf16", seed=T + 7 * A)
 
 
+@pytest.mark.parametrize("T", [1, 33, 100])
+def test_few_rows_many_units_ragged(env, T):
+    """A full SmolLM2 layer stack (768 kv-head units) with ragged and tiny contexts: warp ranges that
+    cross many unit boundaries."""
+    run_case(env, 24, 32, 32, 64, T, 5, "f16", seed=T + 11, layers=[0, 23])
+
+
+def test_few_rows_many_units_d128(env):
+    run_case(env, 80, 8, 32, 128, 65, 1, "bf16", seed=5, layers=[0, 41, 79])
+
+
 def test_few_rows_llama3_8b_4096_one_agent(env, path):
     run_case(env, 32, 8, 32, 128, 4096, 1, "bf16", layers=[0, 17, 31])
 
