@@ -355,12 +355,12 @@ __global__ void __launch_bounds__(32 * kMergeWarps) attend_merge(const float* __
 }
 
 // Merge for the tensor-core partition: blockIdx.x is a segment (kv-head unit x row group of up to 64
-// rows), blockIdx.y a block of 32 of its rows, four rows per warp. The segment's pieces are the slots
+// rows), blockIdx.y a block of 16 of its rows, two rows per warp. The segment's pieces are the slots
 // s + c for the CTAs c whose contiguous tile ranges overlap the segment (at most two for segments
 // longer than a CTA's range, the usual case). Index arithmetic is done once per block, and a warp
 // issues the loads of all its rows' first two pieces (and suffix partials) before using any, so the
 // whole merge costs about one memory round trip per warp.
-constexpr int kMergeRowsPerWarp = 4;
+constexpr int kMergeRowsPerWarp = 2;
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) attend_merge_tc(const float* __restrict__ ws_acc,
                                                                     const float* __restrict__ ws_ml,
@@ -512,7 +512,7 @@ polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float
     cfg.numAttrs = 1;
     cudaError_t e;
     if (lay.nc > 0 && lay.RS > 8) {
-        // many rows per segment and few pieces (the tensor-core partition): four rows per warp
+        // many rows per segment and few pieces (the tensor-core partition): two rows per warp
         constexpr int rows_per_block = kMergeWarps * kMergeRowsPerWarp;
         cfg.gridDim = dim3((unsigned)((int64_t)U * lay.nrg), (unsigned)((lay.RS + rows_per_block - 1) / rows_per_block));
         e = D == 128 ? cudaLaunchKernelEx(&cfg, attend_merge_tc<128>, ws_acc, ws_ml, out, H, A, Hq, R, lay, sfx_acc, sfx_ml)
