@@ -1,7 +1,9 @@
 // Multi-agent decode attention over the shared pool when each kv head has
-// only a few query rows: head_dim 64 with up to 8 rows (SmolLM2-1.7B: one
-// query head per kv head, up to 8 agents) or head_dim 128 with up to 4
-// (Llama-3-8B: one agent, 4 GQA heads).
+// only a few query rows: head_dim 64 with up to 16 rows (SmolLM2-1.7B: one
+// query head per kv head, up to 16 agents) or head_dim 128 with up to 8
+// (Llama-3-8B: one or two agents, 4 GQA heads). Rows go through the score MMA
+// in passes of 8 (d = 64) or 4 (d = 128); a group's key and value operands
+// are converted once and used by every pass.
 //
 // PolyKV abstract ("PolyKV: A Shared Asymmetrically-Compressed KV Cache Pool
 // for Multi-Agent LLM Inference"): the agents read one compressed pool, keys
@@ -56,20 +58,23 @@ constexpr int kGroup = 32;                 // tokens per work item (one value-co
 constexpr float kLog2eW = 1.4426950408889634f;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-template <int D>
+// NP = row passes: each group's keys and value codes are converted once and used for NP * RP rows
+template <int D, int NP>
 struct WCfg {
     static constexpr int NB = D / 32;                  // q8_0 blocks per key vector
     static constexpr int KS = D / 16;                  // K-steps of the score MMA
-    static constexpr int RP = 16 / NB;                 // query rows per score MMA
+    static constexpr int RP = 16 / NB;                 // query rows per score MMA (one pass)
+    static constexpr int ROWS = NP * RP;               // query rows per kv head this configuration takes
     static constexpr int MT = D / 16;                  // M-tiles of the value MMA
     static constexpr int KEY = kGroup * D;             // stage layout (bytes): key codes
     static constexpr int SCL = kGroup * NB * 2;        // block scales
     static constexpr int VCB = D * 12;                 // value-code strings
     static constexpr int NRM = kGroup * 2;             // norms
     static constexpr int STAGE = KEY + SCL + VCB + NRM;
-    static constexpr int WARPS = D == 64 ? 8 : 12;     // warps per CTA
-    static constexpr int STAGES = D == 64 ? 4 : 3;     // ring depth per warp
-    static constexpr int CTAS = D == 64 ? 2 : 1;       // CTAs per SM
+    // two passes hold twice the accumulators and query fragments: fewer, larger-register warps
+    static constexpr int WARPS = NP == 2 ? 8 : (D == 64 ? 8 : 12);   // warps per CTA
+    static constexpr int STAGES = NP == 2 ? 4 : (D == 64 ? 4 : 3);   // ring depth per warp
+    static constexpr int CTAS = NP == 2 ? 1 : (D == 64 ? 2 : 1);     // CTAs per SM
     static constexpr int LUT = 64 * 32 * 4;            // centroid-pair table, one copy per lane
     static constexpr int SMEM = LUT + WARPS * STAGES * STAGE + WARPS * STAGES * 8;
     static_assert(STAGE % 16 == 0 && KEY % 16 == 0 && SCL % 16 == 0 && VCB % 16 == 0, "16-byte bulk copies");
@@ -138,9 +143,9 @@ __device__ __forceinline__ float value_wscale(float nmax) {
     return nmax > 0.0f ? ldexpf(1.0f, 7 - en) : 1.0f;
 }
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_warp_kernel(const WParams P) {
-    using C = WCfg<D>;
+template <int D, int NP, bool BF16>
+__global__ void __launch_bounds__(32 * WCfg<D, NP>::WARPS, WCfg<D, NP>::CTAS) attend_warp_kernel(const WParams P) {
+    using C = WCfg<D, NP>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -228,34 +233,38 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
 
     int64_t unit = u_first;
     int gi = (int)(x0 - u_first * P.ng);
-    float m_run = -INFINITY, crow = 0.0f, wsc = 1.0f;
-    float2 lsum = make_float2(0.0f, 0.0f);
-    float o[C::MT][4];
-    uint32_t qa[C::KS][4];
+    float m_run[NP], crow[NP], wsc = 1.0f;   // per pass: running maximum, logit scale
+    float2 lsum[NP];
+    float o[NP][C::MT][4];
+    uint32_t qa[NP][C::KS][4];
     bool fresh = true;   // the segment's state must be (re)initialised
     bool aborted = false;
     int k = 0;
 
     // end of a segment piece: write this warp's partial (the merge kernel combines the unit's pieces)
     auto finish_piece = [&](int64_t u) {
-        float l = lsum.x + lsum.y;
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
         const int64_t slot = u + gw;   // segment = unit (one row group), piece = this warp's range
-        if (t == 0 && g < C::RP && g < P.R)
-            reinterpret_cast<float2*>(P.ws_ml)[slot * P.R + g] = make_float2(m_run, l);
         const float iw = 1.0f / wsc;
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
+        for (int pp = 0; pp < NP; ++pp) {
+            float l = lsum[pp].x + lsum[pp].y;
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            const int rbase = pp * C::RP;
+            if (t == 0 && g < C::RP && rbase + g < P.R)
+                reinterpret_cast<float2*>(P.ws_ml)[slot * P.R + rbase + g] = make_float2(m_run[pp], l);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = 2 * t + h;
-                if (row < C::RP && row < P.R) {
-                    float* dst = P.ws_acc + (slot * P.R + row) * D + 16 * mt + g;
-                    dst[0] = o[mt][h] * iw;
-                    dst[8] = o[mt][2 + h] * iw;
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = 2 * t + h;
+                    if (row < C::RP && rbase + row < P.R) {
+                        float* dst = P.ws_acc + (slot * P.R + rbase + row) * D + 16 * mt + g;
+                        dst[0] = o[pp][mt][h] * iw;
+                        dst[8] = o[pp][mt][2 + h] * iw;
+                    }
                 }
-            }
+        }
     };
 
     for (; k < n; ++k) {
@@ -263,57 +272,64 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             // a new segment: this lane's query dims [t D/4, (t+1) D/4) of row r_lane, scaled by a power of two
             // so that the row's largest magnitude is in [2^14, 2^15), into the score MMA's A fragments
             const int layer = (int)(unit / P.p.H), kvh = (int)(unit - (int64_t)layer * P.p.H);
-            float xq[D / 4];
 #pragma unroll
-            for (int i = 0; i < D / 4; ++i) xq[i] = 0.0f;
-            if (r_lane < P.R) {
-                const int a = r_lane / P.G, gq = r_lane - a * P.G;
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    P.q + (((int64_t)layer * P.A + a) * P.Hq + kvh * P.G + gq) * D + t * (D / 4));
+            for (int pp = 0; pp < NP; ++pp) {
+                const int rq = pp * C::RP + r_lane;   // this pass's query row of the lane
+                float xq[D / 4];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    const uint4 w = __ldg(src + c);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                for (int i = 0; i < D / 4; ++i) xq[i] = 0.0f;
+                if (rq < P.R) {
+                    const int a = rq / P.G, gq = rq - a * P.G;
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        P.q + (((int64_t)layer * P.A + a) * P.Hq + kvh * P.G + gq) * D + t * (D / 4));
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (BF16) {
-                            xq[8 * c + 2 * e] = __uint_as_float(ws[e] << 16);
-                            xq[8 * c + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
-                        } else {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ws[e]));
-                            xq[8 * c + 2 * e] = f.x;
-                            xq[8 * c + 2 * e + 1] = f.y;
+                    for (int c = 0; c < D / 32; ++c) {
+                        const uint4 w = __ldg(src + c);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (BF16) {
+                                xq[8 * c + 2 * e] = __uint_as_float(ws[e] << 16);
+                                xq[8 * c + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
+                            } else {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ws[e]));
+                                xq[8 * c + 2 * e] = f.x;
+                                xq[8 * c + 2 * e + 1] = f.y;
+                            }
                         }
                     }
                 }
-            }
-            float mx = 0.0f;
+                float mx = 0.0f;
 #pragma unroll
-            for (int i = 0; i < D / 4; ++i) mx = fmaxf(mx, fabsf(xq[i]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            int eq = 0;
-            if (mx > 0.0f) frexpf(mx, &eq);
-            const float fq = mx > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;
-            crow = P.scale_log2 / fq;
+                for (int i = 0; i < D / 4; ++i) mx = fmaxf(mx, fabsf(xq[i]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                int eq = 0;
+                if (mx > 0.0f) frexpf(mx, &eq);
+                const float fq = mx > 0.0f ? ldexpf(1.0f, 15 - eq) : 1.0f;
+                crow[pp] = P.scale_log2 / fq;
 #pragma unroll
-            for (int ks = 0; ks < C::KS; ++ks) {
-                const __half2 h01 = __floats2half2_rn(xq[4 * ks] * fq, xq[4 * ks + 1] * fq);
-                const __half2 h23 = __floats2half2_rn(xq[4 * ks + 2] * fq, xq[4 * ks + 3] * fq);
-                const uint32_t u01 = *reinterpret_cast<const uint32_t*>(&h01);
-                const uint32_t u23 = *reinterpret_cast<const uint32_t*>(&h23);
-                qa[ks][0] = b_lo == bt ? u01 : 0u;
-                qa[ks][1] = b_hi == bt ? u01 : 0u;
-                qa[ks][2] = b_lo == bt ? u23 : 0u;
-                qa[ks][3] = b_hi == bt ? u23 : 0u;
+                for (int ks = 0; ks < C::KS; ++ks) {
+                    const __half2 h01 = __floats2half2_rn(xq[4 * ks] * fq, xq[4 * ks + 1] * fq);
+                    const __half2 h23 = __floats2half2_rn(xq[4 * ks + 2] * fq, xq[4 * ks + 3] * fq);
+                    const uint32_t u01 = *reinterpret_cast<const uint32_t*>(&h01);
+                    const uint32_t u23 = *reinterpret_cast<const uint32_t*>(&h23);
+                    qa[pp][ks][0] = b_lo == bt ? u01 : 0u;
+                    qa[pp][ks][1] = b_hi == bt ? u01 : 0u;
+                    qa[pp][ks][2] = b_lo == bt ? u23 : 0u;
+                    qa[pp][ks][3] = b_hi == bt ? u23 : 0u;
+                }
             }
             const int64_t ju = unit - u_first;
             const float nm = __shfl_sync(0xffffffffu, nm_lane, (int)(ju & 31));
             wsc = value_wscale(ju < 32 ? nm : P.p.nmax[unit]);
-            m_run = -INFINITY;
-            lsum = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+            for (int pp = 0; pp < NP; ++pp) {
+                m_run[pp] = -INFINITY;
+                lsum[pp] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) o[pp][mt][0] = o[pp][mt][1] = o[pp][mt][2] = o[pp][mt][3] = 0.0f;
+            }
             fresh = false;
         }
 
@@ -326,11 +342,14 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
         }
         const uint32_t st = ring_u + (uint32_t)(s * C::STAGE);
 
-        // ---- scores: S^T[(row, block)][token] for tokens 8t + 2i + {0, 1} of this lane's row, n-tile i
-        float sc[4][4];
+        const bool ragged = gi == P.ng - 1 && rem < kGroup;
+        // ---- scores: S^T[(row, block)][token] for tokens 8t + 2i + {0, 1} of this lane's row, n-tile i;
+        //      each key fragment is converted once and used by every pass
+        float sc[NP][4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
+#pragma unroll
+            for (int pp = 0; pp < NP; ++pp) sc[pp][i][0] = sc[pp][i][1] = sc[pp][i][2] = sc[pp][i][3] = 0.0f;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 const uint4 w = lds128(st + koff + (uint32_t)(2 * i * D + 16 * c));
@@ -339,7 +358,8 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
                 for (int e = 0; e < 4; ++e) {
                     uint32_t b0, b1;
                     i8x4_to_h2x2(ws[e], b0, b1);
-                    mma16816(sc[i], qa[4 * c + e], b0, b1);
+#pragma unroll
+                    for (int pp = 0; pp < NP; ++pp) mma16816(sc[pp][i], qa[pp][4 * c + e], b0, b1);
                 }
             }
         }
@@ -374,74 +394,84 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             }
         }
 
-        // scores with the block scales applied (the row's logit scale is applied with the maximum below)
-        float2 y[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            y[i] = __ffma2_rn(s_lo[i], make_float2(sc[i][0], sc[i][1]),
-                              __fmul2_rn(s_hi[i], make_float2(sc[i][2], sc[i][3])));
-            if constexpr (C::NB == 4) {   // the other two blocks of the row are in lane g ^ 4
-                y[i].x += __shfl_xor_sync(0xffffffffu, y[i].x, 16);
-                y[i].y += __shfl_xor_sync(0xffffffffu, y[i].y, 16);
-            }
-        }
-        if (gi == P.ng - 1 && rem < kGroup) {   // the unit's ragged last group: no weight past n_ctx
+        if (ragged) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if (8 * t + 2 * i >= rem) { y[i].x = -INFINITY; nw[i].x = 0.0f; }
-                if (8 * t + 2 * i + 1 >= rem) { y[i].y = -INFINITY; nw[i].y = 0.0f; }
+                if (8 * t + 2 * i >= rem) nw[i].x = 0.0f;
+                if (8 * t + 2 * i + 1 >= rem) nw[i].y = 0.0f;
             }
         }
-        // logits in log2 units relative to the running maximum: y * crow - m
-        const float2 cr = make_float2(crow, crow);
-        float2 xl[4];
-        {
-            const float2 negm = make_float2(-m_run, -m_run);
+        uint32_t pb[NP][4];   // per pass: the value MMA's B fragments
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xl[i] = __ffma2_rn(y[i], cr, negm);
-        }
-        const float xm = fmaxf(fmaxf(fmaxf(xl[0].x, xl[0].y), fmaxf(xl[1].x, xl[1].y)),
-                               fmaxf(fmaxf(xl[2].x, xl[2].y), fmaxf(xl[3].x, xl[3].y)));
-        if (__any_sync(0xffffffffu, xm > 8.0f)) {
-            // rare (always on a segment's first group): raise each row's running maximum to at least the
-            // group's, rescale what the row has accumulated, and redo the relative logits
-            float gm = -INFINITY;
+        for (int pp = 0; pp < NP; ++pp) {
+            // scores with the block scales applied (the row's logit scale is applied with the maximum below)
+            float2 y[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float2 ya = __fmul2_rn(y[i], cr);
-                gm = fmaxf(gm, fmaxf(ya.x, ya.y));
+                y[i] = __ffma2_rn(s_lo[i], make_float2(sc[pp][i][0], sc[pp][i][1]),
+                                  __fmul2_rn(s_hi[i], make_float2(sc[pp][i][2], sc[pp][i][3])));
+                if constexpr (C::NB == 4) {   // the other two blocks of the row are in lane g ^ 4
+                    y[i].x += __shfl_xor_sync(0xffffffffu, y[i].x, 16);
+                    y[i].y += __shfl_xor_sync(0xffffffffu, y[i].y, 16);
+                }
             }
-            gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
-            gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
-            const float m_new = fmaxf(m_run, gm);
-            const float alpha = m_run == -INFINITY ? 0.0f : ex2f(m_run - m_new);
-            m_run = m_new;
-            lsum.x *= alpha;
-            lsum.y *= alpha;
-            // output rows 2t and 2t+1 of this lane's accumulators take the probabilities of lanes 8t and 8t + 4
-            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
-            const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+            if (ragged) {   // the unit's ragged last group: no weight past n_ctx
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                o[mt][0] *= a0;
-                o[mt][1] *= a1;
-                o[mt][2] *= a0;
-                o[mt][3] *= a1;
+                for (int i = 0; i < 4; ++i) {
+                    if (8 * t + 2 * i >= rem) y[i].x = -INFINITY;
+                    if (8 * t + 2 * i + 1 >= rem) y[i].y = -INFINITY;
+                }
             }
-            const float2 negm = make_float2(-m_run, -m_run);
+            // logits in log2 units relative to the running maximum: y * crow - m
+            const float2 cr = make_float2(crow[pp], crow[pp]);
+            float2 xl[4];
+            {
+                const float2 negm = make_float2(-m_run[pp], -m_run[pp]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xl[i] = __ffma2_rn(y[i], cr, negm);
-        }
+                for (int i = 0; i < 4; ++i) xl[i] = __ffma2_rn(y[i], cr, negm);
+            }
+            const float xm = fmaxf(fmaxf(fmaxf(xl[0].x, xl[0].y), fmaxf(xl[1].x, xl[1].y)),
+                                   fmaxf(fmaxf(xl[2].x, xl[2].y), fmaxf(xl[3].x, xl[3].y)));
+            if (__any_sync(0xffffffffu, xm > 8.0f)) {
+                // rare (always on a segment's first group): raise each row's running maximum to at least the
+                // group's, rescale what the row has accumulated, and redo the relative logits
+                float gm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 ya = __fmul2_rn(y[i], cr);
+                    gm = fmaxf(gm, fmaxf(ya.x, ya.y));
+                }
+                gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
+                gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+                const float m_new = fmaxf(m_run[pp], gm);
+                const float alpha = m_run[pp] == -INFINITY ? 0.0f : ex2f(m_run[pp] - m_new);
+                m_run[pp] = m_new;
+                lsum[pp].x *= alpha;
+                lsum[pp].y *= alpha;
+                // output rows 2t and 2t+1 of this lane's accumulators take the probabilities of lanes 8t and 8t + 4
+                const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+                const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    o[pp][mt][0] *= a0;
+                    o[pp][mt][1] *= a1;
+                    o[pp][mt][2] *= a0;
+                    o[pp][mt][3] *= a1;
+                }
+                const float2 negm = make_float2(-m_run[pp], -m_run[pp]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xl[i] = __ffma2_rn(y[i], cr, negm);
+            }
 
-        // probabilities (row sums in fp32) and the value MMA's B fragments P' = p ||v|| w in fp16
-        uint32_t pb[4];
+            // probabilities (row sums in fp32) and the value MMA's B fragments P' = p ||v|| w in fp16
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 pr = make_float2(ex2f(xl[i].x), ex2f(xl[i].y));
-            lsum = __fadd2_rn(lsum, pr);
-            const float2 pv = __fmul2_rn(pr, nw[i]);
-            const __half2 h = __floats2half2_rn(pv.x, pv.y);
-            pb[i] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int i = 0; i < 4; ++i) {
+                const float2 pr = make_float2(ex2f(xl[i].x), ex2f(xl[i].y));
+                lsum[pp] = __fadd2_rn(lsum[pp], pr);
+                const float2 pv = __fmul2_rn(pr, nw[i]);
+                const __half2 h = __floats2half2_rn(pv.x, pv.y);
+                pb[pp][i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
         }
 
         // values: coordinates 16 mt + g and 16 mt + g + 8, tokens 8t .. 8t+7 (k-step j: 8t + 4j + {0, 1, 2, 3});
@@ -457,12 +487,14 @@ __global__ void __launch_bounds__(32 * WCfg<D>::WARPS, WCfg<D>::CTAS) attend_war
             a[1] = lds32(lut_u + (pair_offset<0>(fb) | lane4));
             a[2] = lds32(lut_u + (pair_offset<6>(fa) | lane4));
             a[3] = lds32(lut_u + (pair_offset<6>(fb) | lane4));
-            mma16816(o[mt], a, pb[0], pb[1]);
+#pragma unroll
+            for (int pp = 0; pp < NP; ++pp) mma16816(o[pp][mt], a, pb[pp][0], pb[pp][1]);
             a[0] = lds32(lut_u + (pair_offset<12>(fa) | lane4));
             a[1] = lds32(lut_u + (pair_offset<12>(fb) | lane4));
             a[2] = lds32(lut_u + (pair_offset<18>(fa) | lane4));
             a[3] = lds32(lut_u + (pair_offset<18>(fb) | lane4));
-            mma16816(o[mt], a, pb[2], pb[3]);
+#pragma unroll
+            for (int pp = 0; pp < NP; ++pp) mma16816(o[pp][mt], a, pb[pp][2], pb[pp][3]);
         }
 
         // release the stage (generic reads ordered before the async-proxy refill) and refill it
@@ -501,17 +533,17 @@ int sm_count() {
     return v;
 }
 
-template <int D>
+template <int D, int NP>
 struct WPlan {
     int64_t ng, tt;
     int nw, nctas;
     size_t slots;
 };
 
-template <int D>
-WPlan<D> wplan(const PoolView& p, int64_t n_ctx) {
-    using C = WCfg<D>;
-    WPlan<D> pl;
+template <int D, int NP>
+WPlan<D, NP> wplan(const PoolView& p, int64_t n_ctx) {
+    using C = WCfg<D, NP>;
+    WPlan<D, NP> pl;
     pl.ng = (n_ctx + kGroup - 1) / kGroup;
     pl.tt = (int64_t)p.L * p.H * pl.ng;
     const int64_t warps = (int64_t)sm_count() * C::CTAS * C::WARPS;
@@ -524,18 +556,18 @@ WPlan<D> wplan(const PoolView& p, int64_t n_ctx) {
     return pl;
 }
 
-template <int D>
-size_t warp_workspace(const WPlan<D>& pl, int R) {
+template <int D, int NP>
+size_t warp_workspace(const WPlan<D, NP>& pl, int R) {
     return sizeof(float) * pl.slots * (size_t)R * (size_t)(D + 2);
 }
 
-template <int D, bool BF16>
+template <int D, int NP, bool BF16>
 polykv_status run_warp(const PoolView& p, const void* q, float* out, int A, int Hq, int64_t n_ctx, float scale,
                        void* ws, size_t ws_bytes, cudaStream_t stream, const SuffixArgs* sfx) {
-    using C = WCfg<D>;
+    using C = WCfg<D, NP>;
     const int G = Hq / p.H, R = A * G;
-    const WPlan<D> pl = wplan<D>(p, n_ctx);
-    const size_t need = warp_workspace<D>(pl, R);
+    const WPlan<D, NP> pl = wplan<D, NP>(p, n_ctx);
+    const size_t need = warp_workspace<D, NP>(pl, R);
     if (ws_bytes < need) return set_error(POLYKV_E_BUFFER_TOO_SMALL, "attend: workspace %zu < %zu bytes", ws_bytes, need);
     if (pl.ng > 0x7FFFFFFF) return set_error(POLYKV_E_UNSUPPORTED, "attend: context too long");
     WParams P;
@@ -552,7 +584,7 @@ polykv_status run_warp(const PoolView& p, const void* q, float* out, int A, int 
     P.G = G;
     P.R = R;
     P.scale_log2 = scale * kLog2eW;
-    auto kern = attend_warp_kernel<D, BF16>;
+    auto kern = attend_warp_kernel<D, NP, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "attend_warp: smem attribute: %s", cudaGetErrorString(e));
     kern<<<pl.nctas, 32 * C::WARPS, C::SMEM, stream>>>(P);
@@ -575,11 +607,15 @@ polykv_status run_warp(const PoolView& p, const void* q, float* out, int A, int 
 }  // namespace
 
 bool attend_warp_supported(const PoolView& p, int rows) {
-    return rows >= 1 && ((p.d == 64 && rows <= WCfg<64>::RP) || (p.d == 128 && rows <= WCfg<128>::RP));
+    return rows >= 1 && ((p.d == 64 && rows <= WCfg<64, 2>::ROWS) || (p.d == 128 && rows <= WCfg<128, 2>::ROWS));
 }
 
 size_t attend_warp_workspace(const PoolView& p, int rows, int64_t n_ctx) {
-    return p.d == 64 ? warp_workspace<64>(wplan<64>(p, n_ctx), rows) : warp_workspace<128>(wplan<128>(p, n_ctx), rows);
+    if (p.d == 64)
+        return rows <= WCfg<64, 1>::ROWS ? warp_workspace<64, 1>(wplan<64, 1>(p, n_ctx), rows)
+                                         : warp_workspace<64, 2>(wplan<64, 2>(p, n_ctx), rows);
+    return rows <= WCfg<128, 1>::ROWS ? warp_workspace<128, 1>(wplan<128, 1>(p, n_ctx), rows)
+                                      : warp_workspace<128, 2>(wplan<128, 2>(p, n_ctx), rows);
 }
 
 polykv_status launch_attend_warp(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
@@ -589,11 +625,16 @@ polykv_status launch_attend_warp(const PoolView& p, polykv_dtype dt, const void*
     if (!attend_warp_supported(p, rows))
         return set_error(POLYKV_E_UNSUPPORTED, "warp attend: d=%d rows=%d", p.d, rows);
     const bool bf = dt == POLYKV_BF16;
-    if (p.d == 64)
-        return bf ? run_warp<64, true>(p, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, stream, sfx)
-                  : run_warp<64, false>(p, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, stream, sfx);
-    return bf ? run_warp<128, true>(p, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, stream, sfx)
-              : run_warp<128, false>(p, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, stream, sfx);
+#define POLYKV_RUN_WARP(D_, NP_)                                                                              \
+    return bf ? run_warp<D_, NP_, true>(p, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, stream, sfx) \
+              : run_warp<D_, NP_, false>(p, q, out, n_agents, n_q_heads, n_ctx, scale, ws, ws_bytes, stream, sfx)
+    if (p.d == 64) {
+        if (rows <= WCfg<64, 1>::ROWS) POLYKV_RUN_WARP(64, 1);
+        POLYKV_RUN_WARP(64, 2);
+    }
+    if (rows <= WCfg<128, 1>::ROWS) POLYKV_RUN_WARP(128, 1);
+    POLYKV_RUN_WARP(128, 2);
+#undef POLYKV_RUN_WARP
 }
 
 }  // namespace polykv

@@ -26,14 +26,17 @@ def test_stalled_wait_times_out_and_context_survives():
     pool = pk.Pool(L, H, d, T, "bf16")
     pool.encode(torch.from_numpy(kb.view(np.int16)).cuda(), torch.from_numpy(vb.view(np.int16)).cuda())
     q = torch.from_numpy(qb.view(np.int16)).cuda()
-    old = os.environ.pop("POLYKV_ATTEND_PATH", None)
+    old = os.environ.get("POLYKV_ATTEND_PATH")
+    os.environ["POLYKV_ATTEND_PATH"] = "tc"   # the stall hook is the tensor-core kernel's
     os.environ["POLYKV_TEST_STALL"] = "1"
     try:
         pool.attend(q, T)
         torch.cuda.synchronize()
     finally:
         del os.environ["POLYKV_TEST_STALL"]
-        if old is not None:
+        if old is None:
+            del os.environ["POLYKV_ATTEND_PATH"]
+        else:
             os.environ["POLYKV_ATTEND_PATH"] = old
     with pytest.raises(pk.PolyKVError) as e:
         pool.status()

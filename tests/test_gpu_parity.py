@@ -151,8 +151,9 @@ def test_rows_per_kv_head(env, path, A, G):
 # ---- the warp-level kernel (few rows per kv head): every row count it takes, ragged tails,
 # ranges that cross unit boundaries (full layer stacks), peaky queries
 @pytest.mark.parametrize("T", [1, 31, 33, 65, 129, 257, 1000])
-@pytest.mark.parametrize("d,A,G", [(64, 1, 1), (64, 5, 1), (64, 8, 1), (64, 2, 4), (128, 1, 1), (128, 1, 4),
-                                   (128, 2, 2)])
+@pytest.mark.parametrize("d,A,G", [(64, 1, 1), (64, 5, 1), (64, 8, 1), (64, 2, 4), (64, 3, 3), (64, 12, 1),
+                                   (64, 16, 1), (128, 1, 1), (128, 1, 4), (128, 2, 2), (128, 5, 1), (128, 3, 2),
+                                   (128, 2, 4)])
 def test_few_rows_ragged(env, d, A, G, T):
     run_case(env, 2, 3, 3 * G, d, T, A, "f16" if d == 64 else "bf16", seed=T + 7 * A)
 
@@ -172,11 +173,16 @@ def test_few_rows_llama3_8b_4096_one_agent(env, path):
     run_case(env, 32, 8, 32, 128, 4096, 1, "bf16", layers=[0, 17, 31])
 
 
+def test_few_rows_llama3_8b_4096_two_agents(env, path):
+    """8 query rows per kv head: two score passes over each key group."""
+    run_case(env, 32, 8, 32, 128, 4096, 2, "bf16", layers=[0, 17, 31])
+
+
 def test_few_rows_smollm2_eight_agents_bf16(env):
     run_case(env, 24, 32, 32, 64, 1851, 8, "bf16", layers=[3, 23])
 
 
-@pytest.mark.parametrize("d,A,G", [(64, 5, 1), (128, 1, 4)])
+@pytest.mark.parametrize("d,A,G", [(64, 5, 1), (128, 1, 4), (64, 16, 1), (128, 2, 4)])
 def test_few_rows_very_peaky(env, path, d, A, G):
     run_case(env, 4, 8, 8 * G, d, 1500, A, "f16" if d == 64 else "bf16", q_mult=40.0)
 
