@@ -69,7 +69,7 @@ static polykv_status compute_regions(const polykv_pool_desc* d, polykv_pool_regi
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Which attention kernel serves a call: the warp-level kernel when a kv head
-// has few query rows (head_dim 64 with up to 8, 128 with up to 4), the
+// has few query rows (head_dim 64 with up to 16, 128 with up to 8), the
 // tensor-core kernel for head_dim 128 and more rows, the CUDA-core kernel
 // otherwise. The environment variable POLYKV_ATTEND_PATH=simt|tc|warp
 // overrides (tc and warp only where supported) so the paths can be checked

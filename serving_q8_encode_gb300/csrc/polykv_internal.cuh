@@ -74,14 +74,14 @@ polykv_status launch_attend_merge(const float* ws_acc, const float* ws_ml, float
                                   int R, int n_slots, const MergeLayout& ml, int D, cudaStream_t st,
                                   const float* sfx_acc = nullptr, const float* sfx_ml = nullptr);
 
-// tensor-core attention path (head_dim 128, up to 64 rows per kv head)
+// tensor-core attention path (head_dim 128, any row count in groups of 64 rows per kv head)
 bool attend_tc_supported(const PoolView& p, int rows);
 size_t attend_tc_workspace(const PoolView& p, int rows, int64_t n_ctx);
 polykv_status launch_attend_tc(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
                                int n_q_heads, int64_t n_ctx, float scale, void* ws, size_t ws_bytes,
                                cudaStream_t stream, const SuffixArgs* sfx = nullptr);
 
-// warp-level attention path for few rows per kv head (head_dim 64 with up to 8 rows, 128 with up to 4)
+// warp-level attention path for few rows per kv head (head_dim 64 with up to 16 rows, 128 with up to 8)
 bool attend_warp_supported(const PoolView& p, int rows);
 size_t attend_warp_workspace(const PoolView& p, int rows, int64_t n_ctx);
 polykv_status launch_attend_warp(const PoolView& p, polykv_dtype dt, const void* q, float* out, int n_agents,
