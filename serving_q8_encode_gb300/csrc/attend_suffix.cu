@@ -192,6 +192,247 @@ __global__ void __launch_bounds__(kSfxThreads) suffix_partial(const uint16_t* __
     }
 }
 
+// ---------------------------------------------------------------- suffix on warp-level MMAs (G <= 8)
+// The suffix is plain bf16 or f16 K/V, so it is read at HBM rate only if every byte goes straight from a
+// wide load into arithmetic. One CTA of four warps takes one (layer, agent, kv head) unit at a time
+// (persistent over units); warp w takes the w-th quarter of the unit's 16-token steps and keeps its
+// online-softmax state in registers; the four warp partials are combined in shared memory.
+//
+// Per 16-token step, with m16n8k16 MMAs in the inputs' own type (products exact, fp32 sums):
+//   scores  S[row][token] = Q[row][dims] . K[token][dims]^T: M = the unit's G query rows (zero-padded
+//           to 16), N = 8 tokens, K = 16 dims per step. The head dimension is permuted identically for
+//           Q and K (the dot product does not change): at k-step s, lane quad position t owns the four
+//           dims D/4 * t + 4s + {0..3}, so each lane reads one contiguous quarter of a key row.
+//   values  O^T[dim][row] += V^T[dim][token] . P[token][row]: the 16 tokens of the K step are the two
+//           score n-tiles, so the B fragment is the lane's own score accumulators turned into
+//           probabilities; the rows (dims) are permuted so that a lane's slice of a value row is D/8
+//           contiguous dims, and each A register pairs two tokens of one dim (one byte permute).
+//           P goes in as a high and a low part in the input type (two MMAs), so the probabilities
+//           carry about 2^-17 relative error instead of the type's own rounding.
+constexpr int kSmWarps = 4;
+constexpr int kSmThreads = 32 * kSmWarps;
+
+template <bool BF16>
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    if constexpr (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+// two floats -> one register of the input type (round to nearest), and back
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_rn(float lo, float hi) {
+    if constexpr (BF16) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&v);
+    } else {
+        const __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&v);
+    }
+}
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    else return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+__device__ __forceinline__ float ex2a(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kSmThreads, 3) suffix_mma(const uint16_t* __restrict__ q,
+                                                            const uint16_t* __restrict__ sk,
+                                                            const uint16_t* __restrict__ sv, int H, int Hq, int64_t S,
+                                                            int64_t n_units, float scale_log2,
+                                                            float* __restrict__ acc_out, float* __restrict__ ml_out) {
+    constexpr int KS = D / 16;   // score k-steps
+    constexpr int DPT = D / 4;   // key dims per lane quad position
+    constexpr int DV = D / 8;    // value dims per lane group row
+    constexpr int MT = D / 16;   // value m-tiles
+    constexpr int KC = DPT / 8;  // 16-byte key chunks per lane and token
+    constexpr int VC = DV / 8;   // 16-byte value chunks per lane and token
+    __shared__ __align__(16) float pacc[kSmWarps][8][D];
+    __shared__ float pm[kSmWarps][8], pl[kSmWarps][8];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int G = Hq / H;
+    const int64_t nsteps = (S + 15) / 16;
+    const int64_t s0 = warp * nsteps / kSmWarps, s1 = (warp + 1) * nsteps / kSmWarps;
+
+    for (int64_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+        const int64_t la = unit / H;   // layer * A + agent
+        const int h = (int)(unit - la * H);
+        const uint16_t* kb = sk + unit * S * D;
+        const uint16_t* vb = sv + unit * S * D;
+        // query fragments of row g (rows G..15 are zero): k-step s takes words 2s (a0) and 2s + 1 (a2)
+        uint32_t qa[KS][2];
+        if (g < G) {
+            const uint4* qp = reinterpret_cast<const uint4*>(q + ((la * Hq) + h * G + g) * D + DPT * t);
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+                const uint4 w = __ldg(qp + c);
+                qa[2 * c][0] = w.x;
+                qa[2 * c][1] = w.y;
+                qa[2 * c + 1][0] = w.z;
+                qa[2 * c + 1][1] = w.w;
+            }
+        } else {
+#pragma unroll
+            for (int s = 0; s < KS; ++s) qa[s][0] = qa[s][1] = 0u;
+        }
+        float m = -INFINITY, l = 0.0f;
+        float o[MT][4];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+
+        for (int64_t st = s0; st < s1; ++st) {
+            const int64_t tb = st * 16;
+            // keys of tokens tb + 8 jj + g (score n-tile jj, column g): dims DPT t .. DPT t + DPT
+            uint4 kw[2][KC];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int64_t tok = tb + 8 * jj + g;
+                const uint4* kp = reinterpret_cast<const uint4*>(kb + tok * D + DPT * t);
+#pragma unroll
+                for (int c = 0; c < KC; ++c) kw[jj][c] = tok < S ? __ldg(kp + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // values of tokens tb + {2t, 2t + 1, 8 + 2t, 9 + 2t} (value k = 2t, 2t+1, 2t+8, 2t+9): dims DV g ..
+            uint4 vw[4][VC];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int64_t tok = tb + (e >> 1) * 8 + 2 * t + (e & 1);
+                const uint4* vp = reinterpret_cast<const uint4*>(vb + tok * D + DV * g);
+#pragma unroll
+                for (int c = 0; c < VC; ++c) vw[e][c] = tok < S ? __ldg(vp + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // scores of row g for tokens tb + 8 jj + 2t + {0, 1}
+            float sc[2][4];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                sc[jj][0] = sc[jj][1] = sc[jj][2] = sc[jj][3] = 0.0f;
+#pragma unroll
+                for (int s = 0; s < KS; ++s)
+                    mma_m16n8k16<BF16>(sc[jj], qa[s][0], 0u, qa[s][1], 0u, word_of(kw[jj][s >> 1], 2 * (s & 1)),
+                                       word_of(kw[jj][s >> 1], 2 * (s & 1) + 1));
+            }
+            float x[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int64_t tok = tb + 8 * jj + 2 * t + e;
+                    x[jj][e] = tok < S ? sc[jj][e] * scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[jj][e]);
+                }
+            // token tb is valid, so the quad's maximum is finite
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mn = fmaxf(m, mx);
+            const bool raise = mn > m;
+            const float alpha = ex2a(m - mn);   // 0 at the first step (m = -inf), 1 when the max holds
+            m = mn;
+            float p[2][2];
+            float ps = 0.0f;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    p[jj][e] = ex2a(x[jj][e] - mn);
+                    ps += p[jj][e];
+                }
+            l = l * alpha + ps;
+            if (__any_sync(0xffffffffu, raise)) {
+                // accumulator rows 2t and 2t + 1 belong to lane quads 2t and 2t + 1
+                const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+                const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    o[i][0] *= a0;
+                    o[i][1] *= a1;
+                    o[i][2] *= a0;
+                    o[i][3] *= a1;
+                }
+            }
+            // B fragments: k = 2t, 2t+1 are this lane's n-tile 0 columns, k = 2t+8, 2t+9 its n-tile 1 columns
+            const uint32_t bh0 = pack_rn<BF16>(p[0][0], p[0][1]), bh1 = pack_rn<BF16>(p[1][0], p[1][1]);
+            const float2 f0 = unpack2<BF16>(bh0), f1 = unpack2<BF16>(bh1);
+            const uint32_t bl0 = pack_rn<BF16>(p[0][0] - f0.x, p[0][1] - f0.y);
+            const uint32_t bl1 = pack_rn<BF16>(p[1][0] - f1.x, p[1][1] - f1.y);
+            // m-tile i: A rows g and g + 8 are dims DV g + 2i and DV g + 2i + 1, i.e. the low and high
+            // halves of word i of each token's slice
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                const uint32_t w0 = word_of(vw[0][i >> 2], i & 3), w1 = word_of(vw[1][i >> 2], i & 3);
+                const uint32_t w2 = word_of(vw[2][i >> 2], i & 3), w3 = word_of(vw[3][i >> 2], i & 3);
+                const uint32_t a0 = prmt(w0, w1, 0x5410u), a1 = prmt(w0, w1, 0x7632u);
+                const uint32_t a2 = prmt(w2, w3, 0x5410u), a3 = prmt(w2, w3, 0x7632u);
+                mma_m16n8k16<BF16>(o[i], a0, a1, a2, a3, bh0, bh1);
+                mma_m16n8k16<BF16>(o[i], a0, a1, a2, a3, bl0, bl1);
+            }
+        }
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        // this warp's partial: o[i] holds rows 2t, 2t+1 at dims DV g + 2i (0, 1) and DV g + 2i + 1 (2, 3)
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            pacc[warp][2 * t][DV * g + 2 * i] = o[i][0];
+            pacc[warp][2 * t + 1][DV * g + 2 * i] = o[i][1];
+            pacc[warp][2 * t][DV * g + 2 * i + 1] = o[i][2];
+            pacc[warp][2 * t + 1][DV * g + 2 * i + 1] = o[i][3];
+        }
+        if (t == 0) {
+            pm[warp][g] = m;   // -inf for a warp with no tokens of this unit
+            pl[warp][g] = l;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < G * D; idx += kSmThreads) {
+            const int r = idx / D, col = idx - r * D;
+            float M = pm[0][r];
+#pragma unroll
+            for (int w = 1; w < kSmWarps; ++w) M = fmaxf(M, pm[w][r]);
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kSmWarps; ++w)
+                if (pm[w][r] != -INFINITY) sum += pacc[w][r][col] * ex2a(pm[w][r] - M);
+            acc_out[((la * Hq) + h * G + r) * D + col] = sum;
+        }
+        if (tid < G) {
+            float M = pm[0][tid];
+#pragma unroll
+            for (int w = 1; w < kSmWarps; ++w) M = fmaxf(M, pm[w][tid]);
+            float L = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kSmWarps; ++w)
+                if (pm[w][tid] != -INFINITY) L += pl[w][tid] * ex2a(pm[w][tid] - M);
+            ml_out[((la * Hq) + h * G + tid) * 2] = M;
+            ml_out[((la * Hq) + h * G + tid) * 2 + 1] = L;
+        }
+        __syncthreads();   // the partials' shared memory is reused by the next unit
+    }
+}
+
 // ---------------------------------------------------------------- query-chunk mode
 // Each agent's chunk of C query tokens carries its own keys/values; query token c sees the agent's
 // chunk tokens 0..c (plus the pool, merged later). One block per (layer, agent, kv head, block of 32
@@ -352,10 +593,28 @@ polykv_status launch_suffix_partial(const SuffixArgs& a, int L, int A, int H, in
 }
 
 template <int D, bool BF16>
+polykv_status launch_suffix_mma(const SuffixArgs& a, int L, int A, int H, int Hq, float sl, cudaStream_t st) {
+    auto kern = suffix_mma<D, BF16>;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSmThreads, 0);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    const int64_t units = (int64_t)L * A * H;
+    const int64_t cap = (int64_t)device_sm_count() * per_sm;
+    const unsigned blocks = (unsigned)(units < cap ? units : cap);
+    kern<<<blocks, kSmThreads, 0, st>>>(static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
+                                        static_cast<const uint16_t*>(a.v), H, Hq, a.len, units, sl, a.acc, a.ml);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "suffix launch: %s", cudaGetErrorString(e));
+    return POLYKV_OK;
+}
+
+template <int D, bool BF16>
 polykv_status run_suffix(const SuffixArgs& a, int L, int A, int H, int Hq, float scale, cudaStream_t st) {
     const int G = Hq / H;
     const float sl = scale * 1.4426950408889634f;
-    if (G <= 4) return launch_suffix_partial<D, 4, BF16>(a, L, A, H, Hq, sl, st);
+    if (a.len < 1) return set_error(POLYKV_E_INVAL, "suffix: length %lld", (long long)a.len);
+    // up to 8 query rows per kv head on the warp-level MMAs; more rows on the CUDA-core kernel
+    if (G <= 8) return launch_suffix_mma<D, BF16>(a, L, A, H, Hq, sl, st);
     return launch_suffix_partial<D, 16, BF16>(a, L, A, H, Hq, sl, st);
 }
 

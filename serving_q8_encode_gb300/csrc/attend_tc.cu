@@ -189,15 +189,16 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 
-// OR of `pred` over the `n` threads of named barrier `id`, which all wait here.
+// OR of `pred` over the `n` threads of named barrier `id`, which all wait here. Only the vote is
+// needed from it (shared-memory hand-offs use their own barriers), so it carries no compiler memory
+// clobber and the loads and stores around it may be scheduled across it.
 __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool pred) {
     uint32_t r;
     asm volatile(
         "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.or.pred q, %2, %3, p;\n"
         " selp.u32 %0, 1, 0, q;\n}"
         : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(n)
-        : "memory");
+        : "r"((uint32_t)pred), "r"(id), "r"(n));
     return r != 0;
 }
 
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
             const uint8_t* stgp1 = sm + kSmRing + (uint32_t)st_1 * kStageBytes;
             // queries of tile i+2's segment, if it starts one (loaded now, stored at the end)
             const bool qprep = (i + 2 < n) && ti_2 == 0;
-            uint4 qr[2] = {};
+            uint4 qr[2];
             if (qprep) {
                 Cursor cq;
                 seg_cursor(c0.seg + k_2, cq);
@@ -735,7 +736,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
             uint32_t vv[16];
             value_pairs(w0, w1, w2, lut_lane, vv);
 
-            // -- f. after MMA2(i-1): write out a finished piece's O, rescale O, publish V'(i), P'(i)
+            {
+                // P'(i) into buffer i & 1, last read by MMA2(i-2), which this thread saw complete in the
+                // previous iteration. P'^T rows (token t) of the MN-major B operand, 128-byte swizzle:
+                // this thread's 16 rows are the 16-byte chunks 2g and 2g+1 of the token's 128-byte row
+                const uint32_t prow = sm_u + kSmP + (uint32_t)(i & 1) * 16384u + (uint32_t)t * 128u;
+                st_shared16(prow + ((uint32_t)((2 * g) ^ (t & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+                st_shared16(prow + ((uint32_t)((2 * g + 1) ^ (t & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+            }
+            // -- f. after MMA2(i-1): write out a finished piece's O, rescale O, publish V'(i)
             if (i > 0) {
                 tc::mbar_wait(b_m2, (uint32_t)((i - 1) & 1), abortp, kTimeoutNs);
                 tc::fence_after();
@@ -762,13 +771,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
                 tc::tmem_st16(lane_addr + kColO + 16u * g, ox);
             }
             tc::tmem_st16(lane_addr + kColV + 16u * g, vv);
-            {
-                // P'^T rows (token t) of the MN-major B operand, 128-byte swizzle: this thread's 16 rows
-                // are the 16-byte chunks 2g and 2g+1 of the token's 128-byte row
-                const uint32_t prow = sm_u + kSmP + (uint32_t)(i & 1) * 16384u + (uint32_t)t * 128u;
-                st_shared16(prow + ((uint32_t)((2 * g) ^ (t & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
-                st_shared16(prow + ((uint32_t)((2 * g + 1) ^ (t & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
-            }
             tc::wait_st();
             tc::fence_before();
             // orders this thread's reads of ring stage i (and P' writes) before the async proxy: the MMA
@@ -828,10 +830,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
             const uint64_t bp0 = tc::sdesc(sm_u + kSmP, 16384, 1024);
             const uint32_t tS = tbase + kColS, tK = tbase + kColK, tV = tbase + kColV, tO = tbase + kColO;
             const uint32_t b_sfull = tc::smem_u32(&M.sfull), b_m2 = tc::smem_u32(&M.mma2done);
-            // bounded wait by lane 0, result broadcast so that the warp stays converged
+            // bounded wait by lane 0, result broadcast so that the warp stays converged; the issuer polls
+            // (test_wait) instead of suspending, because its wake-up latency sits on the per-tile chain
             auto wait0 = [&](uint64_t& bar, uint32_t ph) -> bool {
                 int ok = 1;
-                if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&bar), ph, abortp, kTimeoutNs) ? 1 : 0;
+                if (lane == 0) ok = tc::mbar_poll(tc::smem_u32(&bar), ph, abortp, kTimeoutNs) ? 1 : 0;
                 return __shfl_sync(0xffffffffu, ok, 0) != 0;
             };
             int ti = c0.ti;
@@ -918,14 +921,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) attend_tc_kernel(const __grid_c
     if (tid == 0 && M.abort) atomicOr(P.p.status, 1u);
 }
 
-// SM count of the current device (read per call: cheap, and right for every device of a process)
-int num_sms() {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
-    return v;
-}
-
 struct TcPlan {
     int64_t nt, tt, nseg;
     int nctas, nrg, RS;
@@ -939,7 +934,7 @@ TcPlan plan(const PoolView& p, int rows, int64_t n_ctx) {
     pl.RS = pl.nrg > 1 ? kNR : rows;
     pl.nseg = (int64_t)p.L * p.H * pl.nrg;
     pl.tt = pl.nseg * pl.nt;
-    const int64_t sms = num_sms();
+    const int64_t sms = device_sm_count();
     pl.nctas = (int)(pl.tt < sms ? pl.tt : sms);
     pl.slots = (size_t)(pl.nseg + pl.nctas);
     return pl;

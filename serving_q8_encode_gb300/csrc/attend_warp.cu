@@ -525,14 +525,6 @@ __global__ void __launch_bounds__(32 * WCfg<D, NP>::WARPS, WCfg<D, NP>::CTAS) at
     if (lane == 0) atomicOr(P.p.status, 1u);
 }
 
-// SM count of the current device
-int sm_count() {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
-    return v;
-}
-
 template <int D, int NP>
 struct WPlan {
     int64_t ng, tt;
@@ -546,11 +538,11 @@ WPlan<D, NP> wplan(const PoolView& p, int64_t n_ctx) {
     WPlan<D, NP> pl;
     pl.ng = (n_ctx + kGroup - 1) / kGroup;
     pl.tt = (int64_t)p.L * p.H * pl.ng;
-    const int64_t warps = (int64_t)sm_count() * C::CTAS * C::WARPS;
+    const int64_t warps = (int64_t)device_sm_count() * C::CTAS * C::WARPS;
     pl.nw = (int)(pl.tt < warps ? pl.tt : warps);
     // ranges are numbered across CTAs first (range = warp * grid + CTA): with one CTA per SM slot even
     // a small number of ranges is spread over every SM
-    const int64_t slots_ctas = (int64_t)sm_count() * C::CTAS;
+    const int64_t slots_ctas = (int64_t)device_sm_count() * C::CTAS;
     pl.nctas = (int)(pl.nw < slots_ctas ? pl.nw : slots_ctas);
     pl.slots = (size_t)((int64_t)p.L * p.H + pl.nw);
     return pl;

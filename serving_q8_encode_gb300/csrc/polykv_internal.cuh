@@ -10,6 +10,14 @@
 
 namespace polykv {
 
+// SM count of the current device (read per call: cheap, and right for every device of a process)
+inline int device_sm_count() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    return v;
+}
+
 constexpr int kQ8Block = 32;       // q8_0 block length along head_dim
 constexpr int kTokenAlign = 128;   // pool capacity is rounded to this many tokens
 

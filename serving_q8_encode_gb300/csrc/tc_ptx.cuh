@@ -164,6 +164,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// The same bounded wait by polling with test_wait (the thread never suspends): for a thread whose
+// reaction time to the phase is on a critical path. The abort flag and the clock are read every 256
+// polls.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t k = 1;; ++k) {
+        if (mbar_test(bar, parity)) return true;
+        if ((k & 255u) == 0u) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > timeout_ns) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
     float r;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));

@@ -353,6 +353,22 @@ def test_suffix_peaky(env, path):
     run_suffix_case(env, 1, 2, 8, 128, 500, 2, 128, "bf16", q_mult=8.0)
 
 
+def test_suffix_very_peaky(env):
+    """q x 40: one suffix or pool key takes almost all the weight (the suffix's probabilities go into the
+    value MMA as a high and a low part; this is where their rounding would show)."""
+    run_suffix_case(env, 1, 2, 8, 128, 500, 2, 128, "bf16", q_mult=40.0)
+
+
+def test_suffix_long_fp16_d64(env):
+    """A 1,000-token suffix: each of the four warps of a unit runs many 16-token steps (d = 64, f16)."""
+    run_suffix_case(env, 1, 8, 32, 64, 300, 3, 1000, "f16", seed=4)
+
+
+def test_suffix_sixteen_rows_per_kv_head(env):
+    """16 query heads per kv head: more rows than the warp-level suffix kernel takes (CUDA-core kernel)."""
+    run_suffix_case(env, 1, 1, 16, 128, 300, 2, 40, "bf16", seed=6)
+
+
 # ---- query-chunk mode: C query tokens per agent, each with its own key/value, causal inside the chunk
 def run_chunk_case(env, L, H, Hq, d, T, A, C, dtype, seed=0, q_mult=1.0):
     pk, torch, c32, b32 = env
