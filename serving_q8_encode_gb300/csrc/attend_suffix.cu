@@ -261,6 +261,127 @@ __device__ __forceinline__ float ex2a(float x) {
     return y;
 }
 
+// One 16-token step (tokens tb .. tb + 15 of one unit's [token][D] key and value rows) of the warp-level
+// MMA attention of up to 8 query rows: loads of tokens < n_tok, scores of this lane's row g, the online
+// softmax update of (m, l) over the tokens the row sees (token < lim), and the value accumulation into o
+// (rows 2t and 2t + 1). The first step a row takes must contain a token it sees.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_step(const uint16_t* __restrict__ kb, const uint16_t* __restrict__ vb, int64_t tb,
+                                         int64_t n_tok, int64_t lim, float scale_log2, const uint32_t (&qa)[D / 16][2],
+                                         float& m, float& l, float (&o)[D / 16][4], int g, int t) {
+    constexpr int KS = D / 16;   // score k-steps
+    constexpr int DPT = D / 4;   // key dims per lane quad position
+    constexpr int DV = D / 8;    // value dims per lane group row
+    constexpr int MT = D / 16;   // value m-tiles
+    constexpr int KC = DPT / 8;  // 16-byte key chunks per lane and token
+    constexpr int VC = DV / 8;   // 16-byte value chunks per lane and token
+    // keys of tokens tb + 8 jj + g (score n-tile jj, column g): dims DPT t .. DPT t + DPT
+    uint4 kw[2][KC];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int64_t tok = tb + 8 * jj + g;
+        const uint4* kp = reinterpret_cast<const uint4*>(kb + tok * D + DPT * t);
+#pragma unroll
+        for (int c = 0; c < KC; ++c) kw[jj][c] = tok < n_tok ? __ldg(kp + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // values of tokens tb + {2t, 2t + 1, 8 + 2t, 9 + 2t} (value k = 2t, 2t+1, 2t+8, 2t+9): dims DV g ..
+    uint4 vw[4][VC];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int64_t tok = tb + (e >> 1) * 8 + 2 * t + (e & 1);
+        const uint4* vp = reinterpret_cast<const uint4*>(vb + tok * D + DV * g);
+#pragma unroll
+        for (int c = 0; c < VC; ++c) vw[e][c] = tok < n_tok ? __ldg(vp + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // scores of row g for tokens tb + 8 jj + 2t + {0, 1}
+    float sc[2][4];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        sc[jj][0] = sc[jj][1] = sc[jj][2] = sc[jj][3] = 0.0f;
+#pragma unroll
+        for (int s = 0; s < KS; ++s)
+            mma_m16n8k16<BF16>(sc[jj], qa[s][0], 0u, qa[s][1], 0u, word_of(kw[jj][s >> 1], 2 * (s & 1)),
+                               word_of(kw[jj][s >> 1], 2 * (s & 1) + 1));
+    }
+    float x[2][2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int64_t tok = tb + 8 * jj + 2 * t + e;
+            x[jj][e] = tok < lim ? sc[jj][e] * scale_log2 : -INFINITY;
+            mx = fmaxf(mx, x[jj][e]);
+        }
+    // a row sees token 0 at its first step, so m is finite from then on; a later step whose tokens the
+    // row cannot see leaves m unchanged (mx = -inf) and adds p = 0
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m, mx);
+    const bool raise = mn > m;
+    const float alpha = ex2a(m - mn);   // 0 at the first step (m = -inf), 1 when the max holds
+    m = mn;
+    float p[2][2];
+    float ps = 0.0f;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            p[jj][e] = ex2a(x[jj][e] - mn);
+            ps += p[jj][e];
+        }
+    l = l * alpha + ps;
+    if (__any_sync(0xffffffffu, raise)) {
+        // accumulator rows 2t and 2t + 1 belong to lane quads 2t and 2t + 1
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            o[i][0] *= a0;
+            o[i][1] *= a1;
+            o[i][2] *= a0;
+            o[i][3] *= a1;
+        }
+    }
+    // B fragments: k = 2t, 2t+1 are this lane's n-tile 0 columns, k = 2t+8, 2t+9 its n-tile 1 columns
+    const uint32_t bh0 = pack_rn<BF16>(p[0][0], p[0][1]), bh1 = pack_rn<BF16>(p[1][0], p[1][1]);
+    const float2 f0 = unpack2<BF16>(bh0), f1 = unpack2<BF16>(bh1);
+    const uint32_t bl0 = pack_rn<BF16>(p[0][0] - f0.x, p[0][1] - f0.y);
+    const uint32_t bl1 = pack_rn<BF16>(p[1][0] - f1.x, p[1][1] - f1.y);
+    // m-tile i: A rows g and g + 8 are dims DV g + 2i and DV g + 2i + 1, i.e. the low and high
+    // halves of word i of each token's slice
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+        const uint32_t w0 = word_of(vw[0][i >> 2], i & 3), w1 = word_of(vw[1][i >> 2], i & 3);
+        const uint32_t w2 = word_of(vw[2][i >> 2], i & 3), w3 = word_of(vw[3][i >> 2], i & 3);
+        const uint32_t a0 = prmt(w0, w1, 0x5410u), a1 = prmt(w0, w1, 0x7632u);
+        const uint32_t a2 = prmt(w2, w3, 0x5410u), a3 = prmt(w2, w3, 0x7632u);
+        mma_m16n8k16<BF16>(o[i], a0, a1, a2, a3, bh0, bh1);
+        mma_m16n8k16<BF16>(o[i], a0, a1, a2, a3, bl0, bl1);
+    }
+}
+
+// Query fragment of one row (row == nullptr: a zero padding row): k-step s takes the lane's words 2s
+// (a0) and 2s + 1 (a2) of dims D/4 * t .. D/4 * t + D/4 - 1.
+template <int D>
+__device__ __forceinline__ void load_query_frag(const uint16_t* row, int t, uint32_t (&qa)[D / 16][2]) {
+    constexpr int KC = D / 32;   // 16-byte chunks of the lane's quarter
+    if (row) {
+        const uint4* qp = reinterpret_cast<const uint4*>(row + (D / 4) * t);
+#pragma unroll
+        for (int c = 0; c < KC; ++c) {
+            const uint4 w = __ldg(qp + c);
+            qa[2 * c][0] = w.x;
+            qa[2 * c][1] = w.y;
+            qa[2 * c + 1][0] = w.z;
+            qa[2 * c + 1][1] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) qa[s][0] = qa[s][1] = 0u;
+    }
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kSmThreads, 3) suffix_mma(const uint16_t* __restrict__ q,
                                                             const uint16_t* __restrict__ sk,
@@ -268,11 +389,8 @@ __global__ void __launch_bounds__(kSmThreads, 3) suffix_mma(const uint16_t* __re
                                                             int64_t n_units, float scale_log2,
                                                             float* __restrict__ acc_out, float* __restrict__ ml_out) {
     constexpr int KS = D / 16;   // score k-steps
-    constexpr int DPT = D / 4;   // key dims per lane quad position
     constexpr int DV = D / 8;    // value dims per lane group row
     constexpr int MT = D / 16;   // value m-tiles
-    constexpr int KC = DPT / 8;  // 16-byte key chunks per lane and token
-    constexpr int VC = DV / 8;   // 16-byte value chunks per lane and token
     __shared__ __align__(16) float pacc[kSmWarps][8][D];
     __shared__ float pm[kSmWarps][8], pl[kSmWarps][8];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -285,113 +403,15 @@ __global__ void __launch_bounds__(kSmThreads, 3) suffix_mma(const uint16_t* __re
         const int h = (int)(unit - la * H);
         const uint16_t* kb = sk + unit * S * D;
         const uint16_t* vb = sv + unit * S * D;
-        // query fragments of row g (rows G..15 are zero): k-step s takes words 2s (a0) and 2s + 1 (a2)
         uint32_t qa[KS][2];
-        if (g < G) {
-            const uint4* qp = reinterpret_cast<const uint4*>(q + ((la * Hq) + h * G + g) * D + DPT * t);
-#pragma unroll
-            for (int c = 0; c < KC; ++c) {
-                const uint4 w = __ldg(qp + c);
-                qa[2 * c][0] = w.x;
-                qa[2 * c][1] = w.y;
-                qa[2 * c + 1][0] = w.z;
-                qa[2 * c + 1][1] = w.w;
-            }
-        } else {
-#pragma unroll
-            for (int s = 0; s < KS; ++s) qa[s][0] = qa[s][1] = 0u;
-        }
+        load_query_frag<D>(g < G ? q + ((la * Hq) + h * G + g) * D : nullptr, t, qa);
         float m = -INFINITY, l = 0.0f;
         float o[MT][4];
 #pragma unroll
         for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
 
-        for (int64_t st = s0; st < s1; ++st) {
-            const int64_t tb = st * 16;
-            // keys of tokens tb + 8 jj + g (score n-tile jj, column g): dims DPT t .. DPT t + DPT
-            uint4 kw[2][KC];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int64_t tok = tb + 8 * jj + g;
-                const uint4* kp = reinterpret_cast<const uint4*>(kb + tok * D + DPT * t);
-#pragma unroll
-                for (int c = 0; c < KC; ++c) kw[jj][c] = tok < S ? __ldg(kp + c) : make_uint4(0u, 0u, 0u, 0u);
-            }
-            // values of tokens tb + {2t, 2t + 1, 8 + 2t, 9 + 2t} (value k = 2t, 2t+1, 2t+8, 2t+9): dims DV g ..
-            uint4 vw[4][VC];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int64_t tok = tb + (e >> 1) * 8 + 2 * t + (e & 1);
-                const uint4* vp = reinterpret_cast<const uint4*>(vb + tok * D + DV * g);
-#pragma unroll
-                for (int c = 0; c < VC; ++c) vw[e][c] = tok < S ? __ldg(vp + c) : make_uint4(0u, 0u, 0u, 0u);
-            }
-            // scores of row g for tokens tb + 8 jj + 2t + {0, 1}
-            float sc[2][4];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                sc[jj][0] = sc[jj][1] = sc[jj][2] = sc[jj][3] = 0.0f;
-#pragma unroll
-                for (int s = 0; s < KS; ++s)
-                    mma_m16n8k16<BF16>(sc[jj], qa[s][0], 0u, qa[s][1], 0u, word_of(kw[jj][s >> 1], 2 * (s & 1)),
-                                       word_of(kw[jj][s >> 1], 2 * (s & 1) + 1));
-            }
-            float x[2][2];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int64_t tok = tb + 8 * jj + 2 * t + e;
-                    x[jj][e] = tok < S ? sc[jj][e] * scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[jj][e]);
-                }
-            // token tb is valid, so the quad's maximum is finite
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mn = fmaxf(m, mx);
-            const bool raise = mn > m;
-            const float alpha = ex2a(m - mn);   // 0 at the first step (m = -inf), 1 when the max holds
-            m = mn;
-            float p[2][2];
-            float ps = 0.0f;
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    p[jj][e] = ex2a(x[jj][e] - mn);
-                    ps += p[jj][e];
-                }
-            l = l * alpha + ps;
-            if (__any_sync(0xffffffffu, raise)) {
-                // accumulator rows 2t and 2t + 1 belong to lane quads 2t and 2t + 1
-                const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
-                const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-#pragma unroll
-                for (int i = 0; i < MT; ++i) {
-                    o[i][0] *= a0;
-                    o[i][1] *= a1;
-                    o[i][2] *= a0;
-                    o[i][3] *= a1;
-                }
-            }
-            // B fragments: k = 2t, 2t+1 are this lane's n-tile 0 columns, k = 2t+8, 2t+9 its n-tile 1 columns
-            const uint32_t bh0 = pack_rn<BF16>(p[0][0], p[0][1]), bh1 = pack_rn<BF16>(p[1][0], p[1][1]);
-            const float2 f0 = unpack2<BF16>(bh0), f1 = unpack2<BF16>(bh1);
-            const uint32_t bl0 = pack_rn<BF16>(p[0][0] - f0.x, p[0][1] - f0.y);
-            const uint32_t bl1 = pack_rn<BF16>(p[1][0] - f1.x, p[1][1] - f1.y);
-            // m-tile i: A rows g and g + 8 are dims DV g + 2i and DV g + 2i + 1, i.e. the low and high
-            // halves of word i of each token's slice
-#pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                const uint32_t w0 = word_of(vw[0][i >> 2], i & 3), w1 = word_of(vw[1][i >> 2], i & 3);
-                const uint32_t w2 = word_of(vw[2][i >> 2], i & 3), w3 = word_of(vw[3][i >> 2], i & 3);
-                const uint32_t a0 = prmt(w0, w1, 0x5410u), a1 = prmt(w0, w1, 0x7632u);
-                const uint32_t a2 = prmt(w2, w3, 0x5410u), a3 = prmt(w2, w3, 0x7632u);
-                mma_m16n8k16<BF16>(o[i], a0, a1, a2, a3, bh0, bh1);
-                mma_m16n8k16<BF16>(o[i], a0, a1, a2, a3, bl0, bl1);
-            }
-        }
+        for (int64_t st = s0; st < s1; ++st)
+            mma_step<D, BF16>(kb, vb, st * 16, S, S, scale_log2, qa, m, l, o, g, t);
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
         // this warp's partial: o[i] holds rows 2t, 2t+1 at dims DV g + 2i (0, 1) and DV g + 2i + 1 (2, 3)
@@ -430,6 +450,70 @@ __global__ void __launch_bounds__(kSmThreads, 3) suffix_mma(const uint16_t* __re
             ml_out[((la * Hq) + h * G + tid) * 2 + 1] = L;
         }
         __syncthreads();   // the partials' shared memory is reused by the next unit
+    }
+}
+
+// ---------------------------------------------------------------- query-chunk mode on warp-level MMAs
+// The causal part of query-chunk mode (G <= 8): query row r = c G + g of a (layer, agent, kv head) unit
+// (chunk position c, query head g) sees the unit's chunk tokens 0..c. One warp takes 8 consecutive rows of
+// one unit at a time (a task; tasks of one unit are consecutive, so its chunk keys and values are read
+// from HBM once and then from L2) and runs mma_step over 16-token steps up to its last row's position,
+// each row masked at its own position. Each row's partial (running max in log2 units, sum, unnormalised
+// accumulator in the original basis) goes to the suffix slot of virtual agent a C + c.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kSmThreads, 3) chunk_mma(const uint16_t* __restrict__ q,
+                                                           const uint16_t* __restrict__ ck,
+                                                           const uint16_t* __restrict__ cv, int H, int Hq, int64_t C,
+                                                           int64_t n_units, float scale_log2,
+                                                           float* __restrict__ acc_out, float* __restrict__ ml_out) {
+    constexpr int KS = D / 16;
+    constexpr int DV = D / 8;
+    constexpr int MT = D / 16;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int G = Hq / H;
+    const int64_t rows = C * G;
+    const int64_t nrb = (rows + 7) / 8;
+    const int64_t tasks = n_units * nrb;
+    for (int64_t task = (int64_t)blockIdx.x * kSmWarps + (threadIdx.x >> 5); task < tasks;
+         task += (int64_t)gridDim.x * kSmWarps) {
+        const int64_t u = task / nrb, rb = task - u * nrb;
+        const int64_t la = u / H;   // layer * A + agent
+        const int h = (int)(u - la * H);
+        const uint16_t* kb = ck + u * C * D;
+        const uint16_t* vb = cv + u * C * D;
+        // this lane's score row rb * 8 + g: position c_row sees tokens 0..c_row
+        const int64_t row = rb * 8 + g;
+        const bool real = row < rows;
+        const int64_t c_row = real ? row / G : 0;
+        uint32_t qa[KS][2];
+        load_query_frag<D>(real ? q + ((la * C + c_row) * Hq + h * G + (row - c_row * G)) * D : nullptr, t, qa);
+        const int64_t last_row = (rb * 8 + 7 < rows ? rb * 8 + 7 : rows - 1);
+        const int64_t nsteps = last_row / G / 16 + 1;
+        float m = -INFINITY, l = 0.0f;
+        float o[MT][4];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+        for (int64_t st = 0; st < nsteps; ++st)
+            mma_step<D, BF16>(kb, vb, st * 16, C, c_row + 1, scale_log2, qa, m, l, o, g, t);
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        // o[i] holds rows 2t (0, 2) and 2t + 1 (1, 3) at dims DV g + 2i (0, 1) and DV g + 2i + 1 (2, 3)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int64_t ro = rb * 8 + 2 * t + e;
+            if (ro < rows) {
+                const int64_t co = ro / G;
+                float* dst = acc_out + ((la * C + co) * Hq + h * G + (ro - co * G)) * D + DV * g;
+#pragma unroll
+                for (int i = 0; i < MT; ++i)
+                    *reinterpret_cast<float2*>(dst + 2 * i) = make_float2(o[i][e], o[i][2 + e]);
+            }
+        }
+        if (t == 0 && real) {
+            const int64_t orow = (la * C + c_row) * Hq + h * G + (row - c_row * G);
+            ml_out[orow * 2] = m;
+            ml_out[orow * 2 + 1] = l;
+        }
     }
 }
 
@@ -560,9 +644,14 @@ __global__ void __launch_bounds__(kChThreads) chunk_partial(const uint16_t* __re
 }
 
 template <int D, bool BF16>
+polykv_status launch_chunk_mma(const SuffixArgs& a, int L, int A_virtual, int H, int Hq, float sl, cudaStream_t st);
+
+template <int D, bool BF16>
 polykv_status run_chunk(const SuffixArgs& a, int L, int A_virtual, int H, int Hq, float scale, cudaStream_t st) {
     const int G = Hq / H;
     const int64_t C = a.chunk;
+    // up to 8 query heads per kv head on the warp-level MMAs; more on the CUDA-core kernel
+    if (G <= 8) return launch_chunk_mma<D, BF16>(a, L, A_virtual, H, Hq, scale * 1.4426950408889634f, st);
     const int64_t A = A_virtual / C;
     const int64_t nblk_rows = (C * G + kChRows - 1) / kChRows;
     if (nblk_rows > 65535) return set_error(POLYKV_E_UNSUPPORTED, "chunk: %lld query rows per kv head", (long long)(C * G));
@@ -573,6 +662,25 @@ polykv_status run_chunk(const SuffixArgs& a, int L, int A_virtual, int H, int Hq
     chunk_partial<D, BF16><<<grid, kChThreads, smem, st>>>(
         static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k), static_cast<const uint16_t*>(a.v), H, Hq,
         C, scale * 1.4426950408889634f, a.acc, a.ml);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "chunk launch: %s", cudaGetErrorString(e));
+    return POLYKV_OK;
+}
+
+template <int D, bool BF16>
+polykv_status launch_chunk_mma(const SuffixArgs& a, int L, int A_virtual, int H, int Hq, float sl, cudaStream_t st) {
+    auto kern = chunk_mma<D, BF16>;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSmThreads, 0);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    const int64_t C = a.chunk;
+    const int64_t units = (int64_t)L * (A_virtual / C) * H;
+    const int64_t tasks = units * ((C * (Hq / H) + 7) / 8);
+    const int64_t need = (tasks + kSmWarps - 1) / kSmWarps;
+    const int64_t cap = (int64_t)device_sm_count() * per_sm;
+    const unsigned blocks = (unsigned)(need < cap ? need : cap);
+    kern<<<blocks, kSmThreads, 0, st>>>(static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
+                                        static_cast<const uint16_t*>(a.v), H, Hq, C, units, sl, a.acc, a.ml);
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(POLYKV_E_CUDA, "chunk launch: %s", cudaGetErrorString(e));
     return POLYKV_OK;

@@ -411,6 +411,16 @@ def test_chunk_peaky(env, path):
     run_chunk_case(env, 1, 2, 8, 128, 500, 2, 32, "bf16", q_mult=8.0)
 
 
+def test_chunk_very_peaky(env):
+    """q x 40 in chunk mode: the causal part's probabilities go into the value MMA as high and low parts."""
+    run_chunk_case(env, 1, 2, 8, 128, 500, 2, 48, "bf16", q_mult=40.0)
+
+
+def test_chunk_sixteen_rows_per_kv_head(env):
+    """16 query heads per kv head: more rows per chunk position than the warp-level kernel takes."""
+    run_chunk_case(env, 1, 1, 16, 128, 300, 2, 20, "bf16", seed=8)
+
+
 def test_chunk_of_one_equals_one_token_suffix(env):
     """A chunk of length 1 is a one-token private suffix (same keys/values, same softmax)."""
     pk, torch, c32, b32 = env
