@@ -472,7 +472,7 @@ def run_polykv(args, w: synth.Workload):
 
 def run_sweep(args):
     """Encode-only and attend-only throughput at the Llama-3-8B shape over the pages' context lengths
-    and agent counts; one JSON object with the grid (not the driver's single bench line)."""
+    and agent counts; one JSON object with the grid (instead of the single bench line)."""
     import torch
 
     import __graft_entry__
