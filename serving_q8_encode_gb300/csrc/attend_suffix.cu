@@ -4,12 +4,16 @@
 //
 // Each agent appends its own recent tokens after the shared context; those
 // are not part of the compressed pool (the PolyKV abstract's pool is the shared
-// context written once). For every (layer, agent, kv head) this kernel scores
-// the agent's G query heads against its suffix keys and accumulates the suffix
-// values in the ORIGINAL basis, producing one online-softmax partial (running
-// max m in log2 units, sum l, unnormalised accumulator) per query head. The
-// merge kernel combines it with the pool partials (whose accumulators are in
-// the rotated basis) after the pool part's inverse FWHT.
+// context written once). For every (layer, agent, kv head) the kernels here
+// score the agent's query heads against its own keys and accumulate its values
+// in the ORIGINAL basis, producing one online-softmax partial (running max m in
+// log2 units, sum l, unnormalised accumulator) per query row. The merge kernel
+// combines it with the pool partials (whose accumulators are in the rotated
+// basis) after the pool part's inverse FWHT.
+//
+// suffix_mma and chunk_mma (up to 8 query heads per kv head) run on warp-level
+// tensor-core MMAs with register-direct loads; suffix_partial and chunk_partial
+// (CUDA cores, fp32) take more query heads per kv head.
 #include <cmath>
 
 #include "polykv_internal.cuh"
